@@ -1,0 +1,87 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins
+catch each one.  This shows the pins constrain the oracle, not just agree with it."""
+import numpy as np
+import pytest
+
+from oracle import attention, blocks
+from tests import test_oracle_pins as pins
+
+
+def _attention_gqa_modulo(q, K, V, scale):
+    q, K, V = (np.asarray(x, dtype=np.float64) for x in (q, K, V))
+    Hq, D = q.shape
+    Hkv = K.shape[1]
+    out = np.zeros((Hq, D))
+    for h in range(Hq):
+        g = h % Hkv                                   # wrong grouping
+        s = scale * (K[:, g, :] @ q[h])
+        p = np.exp(s - s.max())
+        out[h] = (p @ V[:, g, :]) / p.sum()
+    return out
+
+
+def _attention_no_scale(q, K, V, scale):
+    return _ORIG_ATT(q, K, V, 1.0)
+
+
+def _attention_transposed_kv(q, K, V, scale):
+    return _ORIG_ATT(q, V, K, scale)
+
+
+_ORIG_ATT = attention.decode_attention
+
+
+@pytest.mark.parametrize("bad", [_attention_gqa_modulo, _attention_no_scale,
+                                 _attention_transposed_kv])
+def test_attention_mistakes_are_caught(monkeypatch, bad):
+    monkeypatch.setattr(attention, "decode_attention", bad)
+    with pytest.raises(AssertionError):
+        pins.test_attention_matches_library_sdpa(8, 2, 32, 17)
+
+
+def test_merge_without_rescale_is_caught(monkeypatch):
+    def bad_merge(a, b):
+        (ma, la, Oa), (mb, lb, Ob) = a, b
+        if la == 0:
+            return b
+        if lb == 0:
+            return a
+        return max(ma, mb), la + lb, Oa + Ob           # dropped exp(m - m') factors
+    monkeypatch.setattr(attention, "merge", bad_merge)
+    with pytest.raises(AssertionError):
+        pins.test_split_merge_equals_definition(1000, 16, 512)
+
+
+def test_swapped_slot_encoding_is_caught(monkeypatch):
+    def bad_slot(self, seq, pos):
+        table = self.tables[seq]
+        return (pos % self.block_size) * self.block_size + table[pos // self.block_size]
+    monkeypatch.setattr(blocks.SeqTables, "slot", bad_slot)
+    with pytest.raises((AssertionError, IndexError)):
+        pins.test_append_gather_roundtrip_scrambled()
+
+
+def test_missing_copy_on_write_is_caught(monkeypatch):
+    def reserve_no_cow(self, seq, new_tokens):
+        table = self.tables[seq]
+        need = self.blocks_needed(self.lengths[seq] + int(new_tokens))
+        while len(table) < need:
+            table.append(self.allocator.allocate())
+        return []
+    monkeypatch.setattr(blocks.SeqTables, "reserve", reserve_no_cow)
+    with pytest.raises(AssertionError):
+        pins.test_cow_keeps_parent_history()
+    with pytest.raises(AssertionError):
+        pins.test_fork_cow_p1_numbers()
+
+
+def test_lifo_free_list_is_caught(monkeypatch):
+    def lifo_allocate(self):
+        if not self.free:
+            raise MemoryError("KV block pool exhausted")
+        block = self.free.pop()
+        self.refs[block] = 1
+        return block
+    monkeypatch.setattr(blocks.BlockAllocator, "allocate", lifo_allocate)
+    with pytest.raises(AssertionError):
+        pins.test_allocator_fifo_and_refcounts()
