@@ -1,0 +1,448 @@
+"""Benchmark of paged decode on GB300: one JSON line on stdout.
+
+A step is one pass of the whole hot path over one batch: host table/slot
+resolution and copy-on-write decisions (C++ block manager), then on the
+device pa_copy_blocks, and per layer pa_kv_append + pa_decode.  The default
+workload is the long-context decode: 8 sequences x 32768 tokens, 32 layers of
+independent K/V, fp16, Hq 32 / Hkv 8 / D 128, b 16, 512-token partitions.
+
+  value   effective KV GB/s of the device path: sum over layers and sequences of
+          L * 2 * Hkv * D * sizeof(dtype) bytes per step / device step time.
+          The host plans of all timed steps are made and uploaded before the
+          timed region (inputs resident in HBM).
+  e2e     the same metric through the public API with host buffers: the C++
+          plan of each step, host->device copies of its q / new K / new V rows
+          and tables, the kernels, and the device->host copy of every layer's
+          output, all inside the timed region.
+  --impl reference   times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import configs as wcfg  # noqa: E402
+
+METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq-steps/s at batch×context"
+KERNEL_SOURCES = ["paged_kv_cache_66_gb300/csrc/decode_simt.cuh", "paged_kv_cache_66_gb300/csrc/pa_common.cuh"]
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t)
+    return float(t.item())
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(workload: str):
+    """dram bytes per launch from a committed ncu summary, if taken on this kernel source."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    sha = _kernel_sha()
+    for name in sorted(os.listdir(d)):
+        if not name.endswith(".md"):
+            continue
+        txt = open(os.path.join(d, name)).read()
+        m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+        m_wl = re.search(r"bench_workload:\s*(\S+)", txt)
+        if m_sha and m_tr and m_wl and m_sha.group(1) == sha and m_wl.group(1) == workload:
+            return float(m_tr.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def _workload(cfg: int, steps: int, combo=None):
+    if cfg == 3:
+        return wcfg.config3(steps=steps)
+    if cfg == 2:
+        return wcfg.config2(steps=steps)
+    if cfg == 4:
+        return wcfg.config4(steps=steps)
+    if cfg == 5:
+        D, G, b, dt = combo
+        return wcfg.config5(D=D, G=G, b=b, dtype=dt, steps=steps)
+    return wcfg.config1()
+
+
+def _kv_bytes(wl, lens) -> int:
+    return int(np.sum(np.asarray(lens, dtype=np.int64))) * 2 * wl.Hkv * wl.D * wl.elt
+
+
+def _alg_bytes_decode(wl, plan) -> int:
+    """Algorithmic bytes of one pa_decode launch: K/V history + q + out + block
+    tables + lengths (scratch traffic of the split is not algorithmic)."""
+    B = len(plan.uids)
+    tbl = int(np.sum((np.asarray(plan.lens, dtype=np.int64) + wl.b - 1) // wl.b)) * 4
+    return _kv_bytes(wl, plan.lens) + 2 * B * wl.Hq * wl.D * wl.elt + tbl + 4 * B
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from oracle import attention as oatt
+    from oracle import driver as odriver
+    # Bounded sample: one sequence of layer 0 per step, the oracle gathering the
+    # history through its own pool and table, then the fp64 definition.  For the
+    # long-context workload only the sampled sequence is built.
+    wl = wcfg.config3(steps=1, layers=1, batch=1) if args.config == 3 else _workload(args.config, 1, args.combo)
+    ora = odriver.OracleRun(wl, pools=True, layers=[0])
+    ora.run_setup()
+    rec = ora.run_step_ops(0)[-1]
+    q = wcfg.q_rows(wl, 0, rec["step"], list(range(len(rec["uids"])))).double().numpy()
+    B = len(rec["uids"])
+
+    def one(i):
+        r = i % B
+        t0 = time.perf_counter()
+        oatt.paged_decode(q[r], ora.k_pool[0], ora.v_pool[0], rec["tables"][r], rec["lens"][r], wl.b, wl.scale)
+        return time.perf_counter() - t0, _kv_bytes(wl, [rec["lens"][r]])
+
+    for i in range(args.warmup):
+        one(i)
+    tt, bb = 0.0, 0
+    for i in range(args.steps):
+        t, b = one(args.warmup + i)
+        tt += t
+        bb += b
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    val = bb / tt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": "one sequence of layer 0 per step"},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one {wl.name} sequence x layer 0 per step, {args.steps} steps"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, budget_s: float = 15.0):
+    """The oracle, as it stands, on a bounded sample of the same workload."""
+    from oracle import attention as oatt
+    from workload import configs as wc
+    L = int(wl.setup_ops[1][2]) + 1 if wl.setup_ops[1][0] == "write" else 4096
+    L = min(L, 32768)
+    # a single-sequence pool built from the workload's token contents
+    nb = -(-L // wl.b)
+    t0 = time.perf_counter()
+    pos = np.arange(L, dtype=np.int64)
+    owners = wl.content_owners(0, pos)
+    k = wc.kv_rows(wl, 0, "k", owners, pos)
+    v = wc.kv_rows(wl, 0, "v", owners, pos)
+    perm = np.random.default_rng(0).permutation(nb)
+    kp = torch.zeros((nb, wl.Hkv, wl.b, wl.D), dtype=wl.torch_dtype)
+    vp = torch.zeros_like(kp)
+    from oracle import cache_ops
+    slots = perm[pos // wl.b] * wl.b + pos % wl.b
+    cache_ops.append(kp, vp, k, v, slots, wl.b)
+    q = wc.q_rows(wl, 0, 0, [0]).double().numpy()[0]
+    n, tt = 0, 0.0
+    while tt < budget_s and n < 64:
+        t1 = time.perf_counter()
+        oatt.paged_decode(q, kp, vp, perm.tolist(), L, wl.b, wl.scale)
+        tt += time.perf_counter() - t1
+        n += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": n * _kv_bytes(wl, [L]) / tt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} decodes of one {L}-token sequence, layer 0 of {wl.name} (setup {time.perf_counter()-t0-tt:.1f}s untimed)"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, ws, rank, local):
+    from paged_kv_cache_66_gb300 import api
+    from paged_kv_cache_66_gb300.replay import Replay
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    total_steps = args.warmup + args.steps
+    wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
+    rp = Replay(wl, device=dev)
+    rp.run_setup()
+    torch.cuda.synchronize()
+
+    # plans of warm-up + timed steps, uploaded before the timed region
+    plans = [rp.plan_step(i) for i in range(total_steps)]
+    dsteps = [rp.device_step(p) for p in plans]
+    outs = [torch.empty((len(plans[0].uids), wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev) for _ in rp.layers]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    # every timed step reads the whole history (> L2 by far for the long-context workload)
+    for i in range(args.warmup):
+        rp.run_step(dsteps[i], outs)
+    torch.cuda.synchronize()
+    _barrier(ws)
+
+    nL = len(rp.layers)
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps * nL)]
+    clocks = ClockSampler(local)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    t_start.record(stream)
+    for j in range(args.steps):
+        ds = dsteps[args.warmup + j]
+        B, width = ds.tables.shape
+        wsbuf = rp.workspace_for(B, width)
+        if ds.pairs.shape[0]:
+            api.pa_copy_blocks(rp.k_pools, rp.v_pools, ds.pairs)
+            launches += 1
+        for li in range(nL):
+            api.pa_kv_append(ds.k_new[li], ds.v_new[li], rp.k_pools[li], rp.v_pools[li], ds.slots)
+            a, b = ev_dec[j * nL + li]
+            a.record(stream)
+            api.pa_decode(outs[li], ds.q[li], rp.k_pools[li], rp.v_pools[li], ds.tables, ds.lens, wl.scale,
+                          partition_tokens=rp.partition_tokens, workspace=wsbuf if wsbuf.numel() else None)
+            b.record(stream)
+            launches += 2 + (1 if wsbuf.numel() else 0)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clk = clocks.stop()
+    dev_ms = t_start.elapsed_time(t_end)
+    dev_ms_max = _max_over_ranks(dev_ms, ws, dev)
+    kv = sum(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens) for j in range(args.steps)) * nL
+    kv_all = _sum_over_ranks(float(kv), ws, dev)
+    value = kv_all / (dev_ms_max / 1e3) / 1e9
+    B = len(plans[0].uids)
+    seq_steps = B * args.steps * ws / (dev_ms_max / 1e3)
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan) for j in range(args.steps))
+    peak, peak_kind = _peaks()
+    achieved = alg / (dec_avg / 1e3) / 1e9
+    err = api.pa_get_device_error()
+
+    # ---------------- e2e through the public API with host buffers
+    e2e = run_e2e(args, wl, rp, dev, ws)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dev_ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "batch": B, "context": int(np.max(plans[0].lens)), "layers": nL,
+                   "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
+                   "partition_tokens": rp.partition_tokens, "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{ws}"},
+        "seq_steps_per_s": seq_steps,
+        "pct_hbm_peak": 100.0 * value / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _profiled_traffic(wl.name),
+                     "kernel": "pa_decode (partition + merge)", "peak_kind": f"{peak_kind} hbm_gbs",
+                     "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg},
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"]},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "device_error_word": err,
+    }
+    if not args.no_cpu_baseline and ws >= 1 and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, rp, dev, ws):
+    """K steps through the public API with host buffers (pinned), copies timed."""
+    from paged_kv_cache_66_gb300 import api
+    from workload import configs as wc
+    # inputs of the next K steps, created on the host (not timed): positions
+    # advance by one per step for this churn-free workload
+    uids = list(wl.step_ops[rp.steps_done][-1][1])
+    base = np.array([rp.host.length(u) for u in uids], dtype=np.int64)
+    B, nL = len(uids), len(rp.layers)
+    host_in = []
+    for j in range(args.steps):
+        pos = base + j
+        owners = np.array([wl.content_owner(u, int(p)) for u, p in zip(uids, pos)])
+        qs, ks, vs = [], [], []
+        for layer in rp.layers:
+            qs.append(wc.q_rows(wl, layer, rp.steps_done + j, np.arange(B)).pin_memory())
+            ks.append(wc.kv_rows(wl, layer, "k", owners, pos).pin_memory())
+            vs.append(wc.kv_rows(wl, layer, "v", owners, pos).pin_memory())
+        host_in.append((qs, ks, vs))
+    out_host = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype).pin_memory() for _ in range(nL)]
+    stride = max(len(rp.host.table(u)) for u in uids) + args.steps // wl.b + 2
+    # two sets of pinned metadata buffers, reused every other step once their upload is done
+    bufs = [{"tables": torch.zeros((B, stride), dtype=torch.int32).pin_memory(),
+             "lens": torch.zeros(B, dtype=torch.int32).pin_memory(),
+             "slots": torch.zeros(B, dtype=torch.int64).pin_memory(), "ev": None} for _ in range(2)]
+    d_q = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev) for _ in range(nL)]
+    d_k = [torch.empty((B, wl.Hkv, wl.D), dtype=wl.torch_dtype, device=dev) for _ in range(nL)]
+    d_v = [torch.empty_like(x) for x in d_k]
+    d_out = [torch.empty_like(x) for x in d_q]
+    d_tables = torch.empty((B, stride), dtype=torch.int32, device=dev)
+    d_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    d_slots = torch.empty(B, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    h2d = d2h = 0
+    kv = 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for j in range(args.steps):
+        buf = bufs[j % 2]
+        if buf["ev"] is not None:
+            buf["ev"].synchronize()
+        tables, lens, slots = buf["tables"], buf["lens"], buf["slots"]
+        tn, ln, sn = tables.numpy(), lens.numpy(), slots.numpy()
+        pairs, width = rp.host.decode_step(uids, tn, ln, sn)
+        kv += _kv_bytes(wl, ln) * nL
+        d_tables.copy_(tables, non_blocking=True)
+        d_lens.copy_(lens, non_blocking=True)
+        d_slots.copy_(slots, non_blocking=True)
+        buf["ev"] = torch.cuda.Event()
+        buf["ev"].record(stream)
+        h2d += tables.numel() * 4 + lens.numel() * 4 + slots.numel() * 8
+        if len(pairs):
+            d_pairs = torch.as_tensor(pairs).to(dev, non_blocking=False)
+            api.pa_copy_blocks(rp.k_pools, rp.v_pools, d_pairs)
+            h2d += pairs.nbytes
+        qs, ks, vs = host_in[j]
+        wsbuf = rp.workspace_for(B, stride)
+        for li in range(nL):
+            d_q[li].copy_(qs[li], non_blocking=True)
+            d_k[li].copy_(ks[li], non_blocking=True)
+            d_v[li].copy_(vs[li], non_blocking=True)
+            h2d += (qs[li].numel() + ks[li].numel() + vs[li].numel()) * wl.elt
+            api.pa_kv_append(d_k[li], d_v[li], rp.k_pools[li], rp.v_pools[li], d_slots)
+            api.pa_decode(d_out[li], d_q[li], rp.k_pools[li], rp.v_pools[li], d_tables, d_lens, wl.scale,
+                          partition_tokens=rp.partition_tokens, workspace=wsbuf if wsbuf.numel() else None)
+            out_host[li].copy_(d_out[li], non_blocking=True)
+            d2h += d_out[li].numel() * wl.elt
+    t1.record(stream)
+    torch.cuda.synchronize()
+    rp.steps_done += args.steps
+    ms = _max_over_ranks(t0.elapsed_time(t1), ws, dev)
+    kv_all = _sum_over_ranks(float(kv), ws, dev)
+    return {"value": kv_all / (ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d // args.steps,
+            "d2h_bytes_per_step": d2h // args.steps, "ms_per_step": ms / args.steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--combo", type=str, default="128,4,16,bf16", help="config 5: D,G,b,dtype")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    D, G, b, dt = args.combo.split(",")
+    args.combo = (int(D), int(G), int(b), dt)
+    if args.warmup < 3:
+        raise SystemExit("warmup must be >= 3")
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV-cache device library (libpagedkv.so).
+ *
+ * The KV cache of every sequence lives in fixed-size blocks of b tokens taken
+ * from one pool per layer, laid out [num_blocks, kv_heads, b, head_dim]
+ * ("25. Paged attention and prefix caching", section "Paging").  A
+ * per-sequence block table maps logical block j (tokens [j*b, (j+1)*b)) to a
+ * physical block of the pool.  Three device operations act on the pools:
+ *
+ *   pa_kv_append    write each step's new K/V rows into their slots
+ *                   (same page, section "The paged cache": update's scatter)
+ *   pa_copy_blocks  copy-on-write duplication of shared blocks in every layer
+ *                   (same page, "The paged cache": reserve; "Sharing blocks")
+ *   pa_decode       one query per sequence attends over its paged history
+ *                   (same page, "Attention that reads through the table";
+ *                   "Chapter 7 Paged KV Cache and Memory Management", 4.1-4.2,
+ *                   for the blockwise online softmax and the split merge)
+ *
+ * Conventions shared by every call:
+ *   - All tensors are dense, row-major, owned by the caller and resident on
+ *     the current CUDA device unless stated otherwise.  The library allocates
+ *     no memory, keeps no state except one device error word, and never
+ *     synchronises the stream (pa_get_device_error excepted).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).
+ *   - Arguments are validated on the host before any launch: null pointers,
+ *     non-positive sizes, pointers not 16-byte aligned, and inconsistent
+ *     shapes return PA_ERR_INVALID; shapes that are valid but not compiled
+ *     (head_dim, block size, dtype or query group) return PA_ERR_UNSUPPORTED.
+ *     Nothing is launched in either case.  A failed launch returns PA_ERR_CUDA.
+ *   - Data-dependent errors (a block-table entry or slot outside the pool, a
+ *     sequence length above the table's capacity, a copy pair outside the
+ *     pool) are caught on the device: the offending access is skipped and a
+ *     bit is OR-ed into the device error word, which pa_get_device_error reads.
+ *     No kernel traps or reads out of bounds on bad data.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,        /* bad argument; nothing launched                   */
+    PA_ERR_UNSUPPORTED = 2,    /* valid shape that is not compiled; nothing launched */
+    PA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed       */
+    PA_ERR_DEVICE_CHECK = 4,   /* a device-side check flagged bad data              */
+    PA_ERR_TIMEOUT = 5,        /* a bounded device wait gave up                     */
+    PA_ERR_POOL_EXHAUSTED = 6, /* host block manager: no free block (MemoryError)   */
+    PA_ERR_OVER_RELEASE = 7,   /* host block manager: refcount already 0            */
+    PA_ERR_EXISTS = 8,         /* host block manager: sequence id already exists    */
+    PA_ERR_NOT_FOUND = 9       /* host block manager: unknown sequence id           */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_F32 = 0,
+    PA_F16 = 1,
+    PA_BF16 = 2
+} pa_dtype;
+
+/* Bits of the device error word (see pa_get_device_error). */
+#define PA_DEVERR_SLOT 1         /* pa_kv_append: slot >= num_blocks * b        */
+#define PA_DEVERR_TABLE 2        /* pa_decode: table entry outside [0, num_blocks) */
+#define PA_DEVERR_SEQLEN 4       /* pa_decode: seq_len < 0 or > max_blocks * b  */
+#define PA_DEVERR_PAIR 8         /* pa_copy_blocks: src or dst outside the pool */
+#define PA_DEVERR_TIMEOUT 16     /* a bounded mbarrier wait gave up            */
+
+/*
+ * pa_kv_append -- "reshape_and_cache": scatter new K/V rows into the pools.
+ *
+ *   k, v          [T, Hkv, D] in `dtype`; row t holds token t's key/value.
+ *   k_pool,v_pool [num_blocks, Hkv, b, D] in `dtype`.
+ *   slot_mapping  [T] int64 on the device; slot = physical_block * b + offset,
+ *                 i.e. logical position p of a sequence maps to
+ *                 table[p / b] * b + p % b.  A negative slot skips the row
+ *                 (padding).  Slots of one call must be distinct (otherwise
+ *                 which row lands is unspecified).
+ *   Effect: k_pool[slot / b, h, slot % b, :] = k[t, h, :] (same for v), bit
+ *   exact.  A slot >= num_blocks * b is skipped and flags PA_DEVERR_SLOT.
+ *   Supported: any D with D * sizeof(dtype) a multiple of 16, any b >= 1,
+ *   any dtype.  T may be 0 (no launch).
+ */
+pa_status pa_kv_append(const void* k, const void* v, void* k_pool, void* v_pool,
+                       const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                       int num_kv_heads, int head_dim, int block_size, pa_dtype dtype,
+                       void* stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write: for every pair (src, dst) and every layer,
+ * K_pool[layer][dst] = K_pool[layer][src] and V_pool[layer][dst] = V_pool[layer][src].
+ *
+ *   k_pools, v_pools  HOST arrays of `num_layers` device pointers, one pool per layer.
+ *   pairs             DEVICE int64 [num_pairs, 2] of (src, dst) physical blocks.
+ *                     Destinations must be distinct and disjoint from sources.
+ *   block_bytes       Hkv * b * D * sizeof(dtype): the bytes of one block of one
+ *                     pool; a multiple of 16.
+ *   A pair outside [0, num_blocks) is skipped and flags PA_DEVERR_PAIR.
+ *   num_pairs may be 0 (no launch).
+ */
+pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int num_layers,
+                         const int64_t* pairs, int64_t num_pairs, int64_t num_blocks,
+                         size_t block_bytes, void* stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of fp32 scratch pa_decode needs for a
+ * batch of B sequences with Hq query heads whose block tables have
+ * `max_blocks` columns: per (sequence, query head, partition) one running
+ * max, one normaliser and D partial output values.  Returns 0 when every
+ * sequence fits one partition (max_blocks * b <= partition tokens).
+ * partition_tokens = 0 selects the default (512).
+ */
+size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int max_blocks,
+                                int block_size, int partition_tokens);
+
+/*
+ * pa_decode -- paged decode attention, one query token per sequence.
+ *
+ *   out           [B, Hq, D] in `dtype` (written).
+ *   q             [B, Hq, D] in `dtype`.
+ *   k_pool,v_pool [num_blocks, Hkv, b, D] in `dtype`.
+ *   block_tables  [B, max_blocks] int32; row s lists the physical blocks of
+ *                 sequence s in logical order; entries past ceil(L_s / b) are
+ *                 never read (pad with anything).
+ *   seq_lens      [B] int32; L_s >= 1 tokens of history (the token appended
+ *                 this step included).  L_s = 0 writes a zero row.
+ *   scale         multiplies q . k (the pages use 1 / sqrt(D)).
+ *   Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
+ *   Computes out[s, h] = sum_t softmax_t(scale * q[s,h] . K[t]) V[t] over
+ *   t < L_s with fp32 accumulation, rounded once to `dtype`.
+ *   Sequences longer than `partition_tokens` (0 = 512; a multiple of 16 and
+ *   of b) are split into partitions whose (max, normaliser, partial output)
+ *   go to `workspace` and are merged by a second kernel.
+ *   workspace     device scratch of at least pa_decode_workspace_size(...)
+ *                 bytes, 16-byte aligned; may be NULL when that size is 0.
+ *   Supported: D in {64, 128, 256}; Hq / Hkv in {1, 2, 4, 8}; b a multiple of
+ *   16 up to 256; any dtype.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                    int64_t num_blocks, const int32_t* block_tables, int max_blocks,
+                    const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                    int head_dim, int block_size, float scale, int partition_tokens,
+                    void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_get_device_error -- synchronise `stream`, then read and clear the device
+ * error word of the current device.  *code receives the OR of PA_DEVERR_* bits
+ * raised since the last call (0 when none).  Returns PA_ERR_DEVICE_CHECK when
+ * a data bit is set, PA_ERR_TIMEOUT when only the timeout bit is set, PA_OK
+ * otherwise.
+ */
+pa_status pa_get_device_error(int* code, void* stream);
+
+/* pa_status_string -- static, human-readable name of a status. */
+const char* pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -34,10 +34,9 @@ def gather_history(pool, table, length: int, block_size: int) -> np.ndarray:
     step 3.
     """
     pool = np.asarray(pool.float().numpy() if hasattr(pool, "float") else pool)
-    out = np.zeros((length, pool.shape[1], pool.shape[3]), dtype=np.float64)
-    for t in range(length):
-        out[t] = pool[int(table[t // block_size]), :, t % block_size, :]
-    return out
+    t = np.arange(length)
+    blocks = np.asarray(table, dtype=np.int64)[t // block_size]
+    return pool[blocks, :, t % block_size, :].astype(np.float64)    # [L, Hkv, D]
 
 
 def decode_attention(q, K, V, scale: float) -> np.ndarray:
@@ -98,8 +97,8 @@ def merge(a, b):
 
 def decode_attention_split(q, K, V, scale: float, block_size: int, partition_tokens: int):
     """Online softmax block by block inside each partition, then a merge of the
-    partitions (flash-decoding split), in fp64.  Fully masked partitions are
-    skipped ([P5] 4.2: "it can be skipped directly")."""
+    partitions (flash-decoding split), in fp64.  A partition or block with no
+    valid token contributes nothing and is left out of the merge ([P5] 4.2)."""
     q = np.asarray(q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
     V = np.asarray(V, dtype=np.float64)

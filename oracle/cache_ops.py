@@ -23,14 +23,11 @@ def append(k_pool: torch.Tensor, v_pool: torch.Tensor, k: torch.Tensor, v: torch
     (table[p // b], :, p % b); here the caller has already resolved each
     position to its slot = block * b + offset.  Negative slots are skipped.
     """
-    for t, slot in enumerate(slots):
-        slot = int(slot)
-        if slot < 0:
-            continue
-        block, off = divmod(slot, block_size)
-        for h in range(k.shape[1]):
-            k_pool[block, h, off, :] = k[t, h, :]
-            v_pool[block, h, off, :] = v[t, h, :]
+    slots = torch.as_tensor(slots, dtype=torch.int64).reshape(-1)
+    keep = slots >= 0
+    block, off = slots[keep] // block_size, slots[keep] % block_size
+    k_pool[block, :, off, :] = k[keep]
+    v_pool[block, :, off, :] = v[keep]
 
 
 def copy_blocks(k_pools, v_pools, pairs) -> None:

@@ -1,0 +1,211 @@
+// C ABI of the paged KV-cache device library: argument validation, the
+// device error word, and dispatch to the kernels.  See include/pagedkv.h for
+// the contract of every entry point.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_launch.h"
+
+namespace {
+
+__device__ int g_pa_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultPartition = 512;
+constexpr int kMaxPartition = 8192;
+
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+// Device address of the error word on the current device (looked up once).
+int* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pa_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+inline bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+inline int elt_size(pa_dtype t) {
+    switch (t) {
+        case PA_F32: return 4;
+        case PA_F16: return 2;
+        case PA_BF16: return 2;
+        default: return 0;
+    }
+}
+
+inline pa_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return PA_OK;
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    return PA_ERR_CUDA;
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    int partitions;
+    size_t ml_bytes;
+    size_t total;
+};
+
+WsLayout ws_layout(int batch, int hq, int d, int max_blocks, int b, int part) {
+    WsLayout w{};
+    w.partitions = static_cast<int>(ceil_div(static_cast<int64_t>(max_blocks) * b, part));
+    if (w.partitions <= 1) return w;
+    const size_t rows = static_cast<size_t>(batch) * hq * w.partitions;
+    w.ml_bytes = align256(rows * 2 * sizeof(float));
+    w.total = w.ml_bytes + rows * static_cast<size_t>(d) * sizeof(float);
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slot_mapping,
+                       int64_t num_tokens, int64_t num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       pa_dtype dtype, void* stream) {
+    const int es = elt_size(dtype);
+    if (es == 0 || num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return PA_ERR_INVALID;
+    if (!k_pool || !v_pool || !al(k_pool, 16) || !al(v_pool, 16)) return PA_ERR_INVALID;
+    if ((static_cast<int64_t>(head_dim) * es) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !al(k, 16) || !al(v, 16) || !al(slot_mapping, 8)) return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    return from_cuda(pa::launch_kv_append(k, v, k_pool, v_pool, slot_mapping, num_tokens, num_blocks, num_kv_heads,
+                                          head_dim * es, block_size, err, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int num_layers, const int64_t* pairs,
+                         int64_t num_pairs, int64_t num_blocks, size_t block_bytes, void* stream) {
+    if (!k_pools || !v_pools || num_layers <= 0 || num_pairs < 0 || num_blocks <= 0 || block_bytes == 0 ||
+        block_bytes % 16 != 0)
+        return PA_ERR_INVALID;
+    for (int l = 0; l < num_layers; ++l)
+        if (!k_pools[l] || !v_pools[l] || !al(k_pools[l], 16) || !al(v_pools[l], 16)) return PA_ERR_INVALID;
+    if (num_pairs == 0) return PA_OK;
+    if (!pairs || !al(pairs, 8)) return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    for (int l0 = 0; l0 < num_layers; l0 += pa::kMaxLayersPerLaunch) {
+        const int nl = (num_layers - l0 < pa::kMaxLayersPerLaunch) ? num_layers - l0 : pa::kMaxLayersPerLaunch;
+        pa::PoolPtrs pp{};
+        for (int l = 0; l < nl; ++l) {
+            pp.k[l] = k_pools[l0 + l];
+            pp.v[l] = v_pools[l0 + l];
+        }
+        pa_status st = from_cuda(pa::launch_copy_blocks(pp, nl, pairs, num_pairs, num_blocks, block_bytes, err,
+                                                        static_cast<cudaStream_t>(stream)));
+        if (st != PA_OK) return st;
+    }
+    return PA_OK;
+}
+
+size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int max_blocks, int block_size,
+                                int partition_tokens) {
+    if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks <= 0 || block_size <= 0) return 0;
+    const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    if (part <= 0) return 0;
+    return ws_layout(batch, num_q_heads, head_dim, max_blocks, block_size, part).total;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, float scale, int partition_tokens,
+                    void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+    const int es = elt_size(dtype);
+    if (es == 0 || batch < 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 ||
+        head_dim <= 0 || block_size <= 0 || max_blocks <= 0 || num_blocks <= 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
+    const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    if (part <= 0 || part > kMaxPartition || part % 16 != 0 || part % block_size != 0) return PA_ERR_INVALID;
+    if (static_cast<int64_t>(max_blocks) * block_size > (1LL << 30)) return PA_ERR_INVALID;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return PA_ERR_INVALID;
+    if (!al(out, 16) || !al(q, 16) || !al(k_pool, 16) || !al(v_pool, 16) || !al(block_tables, 4) ||
+        !al(seq_lens, 4))
+        return PA_ERR_INVALID;
+    const WsLayout ws = ws_layout(batch, num_q_heads, head_dim, max_blocks, block_size, part);
+    if (ws.partitions > 1 && (!workspace || !al(workspace, 16) || workspace_bytes < ws.total))
+        return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+
+    pa::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.ws_ml = ws.partitions > 1 ? static_cast<float*>(workspace) : nullptr;
+    p.ws_acc = ws.partitions > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.ml_bytes) : nullptr;
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = num_kv_heads;
+    p.d = head_dim;
+    p.block_size = block_size;
+    p.partition_tokens = part;
+    p.max_partitions = ws.partitions < 1 ? 1 : ws.partitions;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+        case PA_F32: return from_cuda(pa::launch_decode_f32(p, st));
+        case PA_F16: return from_cuda(pa::launch_decode_f16(p, st));
+        case PA_BF16: return from_cuda(pa::launch_decode_bf16(p, st));
+        default: return PA_ERR_INVALID;
+    }
+}
+
+pa_status pa_get_device_error(int* code, void* stream) {
+    if (!code) return PA_ERR_INVALID;
+    *code = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pa_error_word, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_pa_error_word, &zero, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+    *code = v;
+    if (v & ~PA_DEVERR_TIMEOUT) return PA_ERR_DEVICE_CHECK;
+    if (v & PA_DEVERR_TIMEOUT) return PA_ERR_TIMEOUT;
+    return PA_OK;
+}
+
+const char* pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID: return "PA_ERR_INVALID";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE_CHECK: return "PA_ERR_DEVICE_CHECK";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        case PA_ERR_POOL_EXHAUSTED: return "PA_ERR_POOL_EXHAUSTED";
+        case PA_ERR_OVER_RELEASE: return "PA_ERR_OVER_RELEASE";
+        case PA_ERR_EXISTS: return "PA_ERR_EXISTS";
+        case PA_ERR_NOT_FOUND: return "PA_ERR_NOT_FOUND";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

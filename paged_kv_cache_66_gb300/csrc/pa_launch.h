@@ -1,0 +1,50 @@
+// Internal launcher interface between the C ABI (pa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pa {
+
+constexpr int kMaxLayersPerLaunch = 64;
+
+struct PoolPtrs {
+    void* k[kMaxLayersPerLaunch];
+    void* v[kMaxLayersPerLaunch];
+};
+
+// Everything one pa_decode call needs on the device.
+struct DecodeParams {
+    void* out;                  // [B, Hq, D] dtype
+    const void* q;              // [B, Hq, D] dtype
+    const void* k_pool;         // [N, Hkv, b, D] dtype
+    const void* v_pool;
+    const int32_t* block_tables;  // [B, max_blocks]
+    const int32_t* seq_lens;      // [B]
+    float* ws_ml;               // [B, Hq, P, 2] running max (log2 units) and normaliser
+    float* ws_acc;              // [B, Hq, P, D] unnormalised partial outputs
+    int* err;
+    int64_t num_blocks;
+    int max_blocks;
+    int batch;
+    int hq, hkv, d, block_size;
+    int partition_tokens;
+    int max_partitions;         // P = ceil(max_blocks * b / partition_tokens)
+    float scale_log2;           // scale * log2(e)
+};
+
+cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slots,
+                             int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,
+                             int* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(const PoolPtrs& pools, int num_layers, const int64_t* pairs, int64_t num_pairs,
+                               int64_t num_blocks, size_t block_bytes, int* err, cudaStream_t stream);
+
+// Returns cudaErrorNotSupported when (dtype, D, G) has no compiled kernel.
+cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_f16(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,166 @@
+"""Drive a seeded workload through the host block manager and the kernels.
+
+One decode step ("25. Paged attention and prefix caching", section "The paged
+cache", flow per step):
+  1. host: reserve one position per sequence (copy-on-write pairs), slot of
+     the new position, length + 1, padded block tables   (C++ manager)
+  2. device: pa_copy_blocks over every layer for the step's pairs
+  3. device, per layer: pa_kv_append of the new K/V rows, then pa_decode
+The host part of a step is planned separately (``plan_step``) from its device
+part (``run_step``) so that a benchmark can keep the plans of many steps
+resident on the device and time the device path alone.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from workload import configs as wcfg
+
+from . import api
+from .host import HostBlockManager
+
+
+@dataclass
+class StepPlan:
+    step: int
+    uids: list
+    slots: np.ndarray          # [B] int64
+    pairs: np.ndarray          # [n, 2] int64
+    tables: np.ndarray         # [B, width] int32
+    lens: np.ndarray           # [B] int32
+    positions: np.ndarray      # [B] int64 (position of the appended token)
+
+
+@dataclass
+class DeviceStep:
+    """A step's metadata and inputs, resident on the device."""
+    plan: StepPlan
+    slots: torch.Tensor
+    pairs: torch.Tensor
+    tables: torch.Tensor
+    lens: torch.Tensor
+    q: list                    # per layer [B, Hq, D]
+    k_new: list                # per layer [B, Hkv, D]
+    v_new: list
+
+
+class Replay:
+    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.layers = list(range(wl.layers)) if layers is None else list(layers)
+        self.host = HostBlockManager(wl.num_blocks, wl.b, wl.free_order)
+        shape = (wl.num_blocks, wl.Hkv, wl.b, wl.D)
+        self.k_pools = [torch.zeros(shape, dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
+        self.v_pools = [torch.zeros(shape, dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
+        self.partition_tokens = wl.partition_tokens if partition_tokens is None else partition_tokens
+        self.steps_done = 0
+        self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    # ------------------------------------------------------------------ ops
+    def _copy(self, pairs: np.ndarray):
+        if len(pairs):
+            p = torch.as_tensor(np.asarray(pairs, dtype=np.int64).reshape(-1, 2)).to(self.device)
+            api.pa_copy_blocks(self.k_pools, self.v_pools, p)
+
+    def _write(self, uid: int, n: int):
+        wl = self.wl
+        start = self.host.length(uid)
+        pairs = self.host.reserve(uid, n)
+        slots = self.host.slots(uid, start, n)
+        self._copy(np.array(pairs, dtype=np.int64))
+        pos = np.arange(start, start + n, dtype=np.int64)
+        owners = wl.content_owners(uid, pos)
+        slots_d = torch.as_tensor(slots).to(self.device)
+        chunk = 1 << 14
+        for li, layer in enumerate(self.layers):
+            for c0 in range(0, n, chunk):
+                c1 = min(n, c0 + chunk)
+                k = wcfg.kv_rows(wl, layer, "k", owners[c0:c1], pos[c0:c1], device=self.device)
+                v = wcfg.kv_rows(wl, layer, "v", owners[c0:c1], pos[c0:c1], device=self.device)
+                api.pa_kv_append(k, v, self.k_pools[li], self.v_pools[li], slots_d[c0:c1])
+        self.host.advance(uid, n)
+
+    def apply(self, op):
+        kind = op[0]
+        h = self.host
+        if kind == "create":
+            h.create(op[1])
+        elif kind == "write":
+            self._write(op[1], int(op[2]))
+        elif kind == "fork":
+            h.fork(op[1], op[2])
+        elif kind == "truncate":
+            h.truncate(op[1], op[2])
+        elif kind == "free":
+            h.free(op[1])
+        else:
+            raise ValueError(f"op {kind} is not a setup op")
+
+    def run_setup(self):
+        for op in self.wl.setup_ops:
+            self.apply(op)
+
+    # ------------------------------------------------------------------ steps
+    def plan_step(self, step_index: int) -> StepPlan:
+        """Apply the step's non-decode ops (frees, arrivals with their prompt
+        writes), then the host part of the decode step."""
+        ops = self.wl.step_ops[step_index]
+        plan = None
+        for op in ops:
+            if op[0] != "step":
+                self.apply(op)
+                continue
+            uids = list(op[1])
+            B = len(uids)
+            positions = np.array([self.host.length(u) for u in uids], dtype=np.int64)
+            stride = max(len(self.host.table(u)) for u in uids) + 1
+            tables = np.zeros((B, stride), dtype=np.int32)
+            lens = np.zeros(B, dtype=np.int32)
+            slots = np.zeros(B, dtype=np.int64)
+            pairs, w = self.host.decode_step(uids, tables, lens, slots)
+            plan = StepPlan(self.steps_done, uids, slots, pairs, np.ascontiguousarray(tables[:, :w]), lens,
+                            positions)
+            self.steps_done += 1
+        return plan
+
+    def device_step(self, plan: StepPlan) -> DeviceStep:
+        """Upload the plan and generate the step's q and new K/V rows on the device."""
+        wl, dev = self.wl, self.device
+        owners = np.array([wl.content_owner(u, int(p)) for u, p in zip(plan.uids, plan.positions)])
+        rows = np.arange(len(plan.uids))
+        q, kn, vn = [], [], []
+        for layer in self.layers:
+            q.append(wcfg.q_rows(wl, layer, plan.step, rows, device=dev))
+            kn.append(wcfg.kv_rows(wl, layer, "k", owners, plan.positions, device=dev))
+            vn.append(wcfg.kv_rows(wl, layer, "v", owners, plan.positions, device=dev))
+        return DeviceStep(plan, torch.as_tensor(plan.slots).to(dev),
+                          torch.as_tensor(plan.pairs.reshape(-1, 2)).to(dev),
+                          torch.as_tensor(plan.tables).to(dev), torch.as_tensor(plan.lens).to(dev), q, kn, vn)
+
+    def workspace_for(self, batch: int, max_blocks: int) -> torch.Tensor:
+        wl = self.wl
+        need = api.pa_decode_workspace_size(batch, wl.Hq, wl.D, max_blocks, wl.b, self.partition_tokens)
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def run_step(self, ds: DeviceStep, outs=None, stream=None) -> list:
+        """Device part of one decode step over every layer; returns outputs."""
+        wl = self.wl
+        B, width = ds.tables.shape
+        ws = self.workspace_for(B, width)
+        if ds.pairs.shape[0]:
+            api.pa_copy_blocks(self.k_pools, self.v_pools, ds.pairs, stream=stream)
+        if outs is None:
+            outs = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
+        for li in range(len(self.layers)):
+            api.pa_kv_append(ds.k_new[li], ds.v_new[li], self.k_pools[li], self.v_pools[li], ds.slots,
+                             stream=stream)
+            api.pa_decode(outs[li], ds.q[li], self.k_pools[li], self.v_pools[li], ds.tables, ds.lens, wl.scale,
+                          partition_tokens=self.partition_tokens, workspace=ws if ws.numel() else None,
+                          stream=stream)
+        return outs
