@@ -106,7 +106,7 @@ def _profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -115,7 +115,7 @@ class ClockSampler:
         self.proc = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                          "-lms", "50", "-i", str(gpu_index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -256,6 +256,8 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     total_steps = args.warmup + args.steps
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
+    if args.layers:
+        wl.layers = min(wl.layers, args.layers)
     rp = Replay(wl, device=dev)
     rp.run_setup()
     torch.cuda.synchronize()
@@ -313,7 +315,7 @@ def run_ours(args, ws, rank, local):
     err = api.pa_get_device_error()
 
     # ---------------- e2e through the public API with host buffers
-    e2e = run_e2e(args, wl, rp, dev, ws)
+    e2e = None if args.no_e2e else run_e2e(args, wl, rp, dev, ws)
 
     if rank != 0:
         return
@@ -424,12 +426,14 @@ def run_e2e(args, wl, rp, dev, ws):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--combo", type=str, default="128,4,16,bf16", help="config 5: D,G,b,dtype")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     args = ap.parse_args()
     D, G, b, dt = args.combo.split(",")
     args.combo = (int(D), int(G), int(b), dt)
