@@ -147,6 +147,35 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
                     void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory: the same arguments minus the workspace, which comes instead from a
+ * fixed array of PA_DECODE_NOALLOC_MAX_BYTES inside this library.  The pages
+ * have no counterpart; it exists because some callers (an application that
+ * owns all device memory through its own allocator, a loop that must not
+ * allocate after start-up, an ABI consumer without an allocator) cannot
+ * provide scratch.
+ *   - Returns PA_ERR_INVALID, launching nothing, when the call needs more
+ *     scratch than the array holds (pa_decode_workspace_size(...) >
+ *     PA_DECODE_NOALLOC_MAX_BYTES); use pa_decode with caller scratch then.
+ *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Calls whose kernels overlap on the GPU (different streams
+ *     without ordering between them) race on it and give wrong results;
+ *     serialise them.  No clearing is needed between ordered calls.
+ *   - The array stays reserved on every GPU that loads this library's device
+ *     code until the process exits.
+ */
+#define PA_DECODE_NOALLOC_MAX_BYTES (16u << 20)
+pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
+                            int64_t num_blocks, const int32_t* block_tables, int max_blocks,
+                            const int32_t* seq_lens, int batch, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, float scale,
+                            int partition_tokens, pa_dtype dtype, void* stream);
+
+/*
  * pa_get_device_error -- synchronise `stream`, then read and clear the device
  * error word of the current device.  *code receives the OR of PA_DEVERR_* bits
  * raised since the last call (0 when none).  Returns PA_ERR_DEVICE_CHECK when

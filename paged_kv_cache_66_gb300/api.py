@@ -17,7 +17,7 @@ from ._lib import DTYPE_IDS, PagedKVError, check, load
 _TORCH_TO_ID = {torch.float32: DTYPE_IDS["f32"], torch.float16: DTYPE_IDS["f16"],
                 torch.bfloat16: DTYPE_IDS["bf16"]}
 
-__all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
+__all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
            "pa_get_device_error", "pa_status_string", "PagedKVError"]
 
 
@@ -106,6 +106,26 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale, partition_t
                         block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, Hkv, D, b,
                         float(scale), int(partition_tokens), ws_ptr, ws_bytes, _dtype_id(k_pool),
                         _stream(stream)), "pa_decode")
+
+
+def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, partition_tokens=0,
+                      stream=None) -> None:
+    """pa_decode with the library's fixed scratch array instead of caller scratch
+    (for callers that cannot allocate device memory); raises PagedKVError
+    (PA_ERR_INVALID) when the batch needs more scratch than the array holds."""
+    lib = load()
+    B, Hq, D = q.shape
+    N, Hkv, b, D2 = k_pool.shape
+    if D2 != D or tuple(out.shape) != tuple(q.shape) or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    dt = k_pool.dtype
+    check(lib.pa_decode_noalloc(_dev(out, "out", dt), _dev(q, "q", dt), _dev(k_pool, "k_pool", dt),
+                                _dev(v_pool, "v_pool", dt), N, _dev(block_tables, "block_tables", torch.int32),
+                                block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, Hkv, D, b,
+                                float(scale), int(partition_tokens), _dtype_id(k_pool), _stream(stream)),
+          "pa_decode_noalloc")
 
 
 def pa_get_device_error(stream=None) -> int:
