@@ -37,7 +37,8 @@ sys.path.insert(0, ROOT)
 from workload import configs as wcfg  # noqa: E402
 
 METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak); seq-steps/s at batch×context"
-KERNEL_SOURCES = ["paged_kv_cache_66_gb300/csrc/decode_simt.cuh", "paged_kv_cache_66_gb300/csrc/pa_common.cuh"]
+KERNEL_SOURCES = ["paged_kv_cache_66_gb300/csrc/decode_mma.cuh", "paged_kv_cache_66_gb300/csrc/decode_merge.cuh",
+                  "paged_kv_cache_66_gb300/csrc/pa_common.cuh"]
 
 
 def _dist():
@@ -254,6 +255,7 @@ def run_ours(args, ws, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    api.pa_set_decode_kernel(args.kernel)
     total_steps = args.warmup + args.steps
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
@@ -331,7 +333,7 @@ def run_ours(args, ws, rank, local):
         "pct_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(wl.name),
-                     "kernel": "pa_decode (partition + merge)", "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": f"pa_decode ({args.kernel} partition + merge)", "peak_kind": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
@@ -434,6 +436,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
     args = ap.parse_args()
     D, G, b, dt = args.combo.split(",")
     args.combo = (int(D), int(G), int(b), dt)

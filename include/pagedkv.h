@@ -176,6 +176,24 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const 
                             int partition_tokens, pa_dtype dtype, void* stream);
 
 /*
+ * pa_set_decode_kernel -- process-wide choice of the pa_decode partition
+ * kernel (both compute the same result within the attention tolerance):
+ *   PA_DECODE_AUTO  (default) tensor cores for fp16/bf16 pools, CUDA cores for fp32;
+ *   PA_DECODE_SIMT  CUDA cores (fp32 FMAs) for every dtype;
+ *   PA_DECODE_MMA   tensor cores (mma m16n8k16, fp32 accumulate, TMA-fed) --
+ *                   pa_decode then returns PA_ERR_UNSUPPORTED for fp32 pools
+ *                   or pools of 2^31 rows (num_blocks * Hkv * b) or more.
+ * Returns PA_ERR_INVALID for any other value.
+ */
+typedef enum pa_decode_kernel {
+    PA_DECODE_AUTO = 0,
+    PA_DECODE_SIMT = 1,
+    PA_DECODE_MMA = 2
+} pa_decode_kernel;
+
+pa_status pa_set_decode_kernel(pa_decode_kernel kernel);
+
+/*
  * pa_get_device_error -- synchronise `stream`, then read and clear the device
  * error word of the current device.  *code receives the OR of PA_DEVERR_* bits
  * raised since the last call (0 when none).  Returns PA_ERR_DEVICE_CHECK when

@@ -18,7 +18,7 @@ _TORCH_TO_ID = {torch.float32: DTYPE_IDS["f32"], torch.float16: DTYPE_IDS["f16"]
                 torch.bfloat16: DTYPE_IDS["bf16"]}
 
 __all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
-           "pa_get_device_error", "pa_status_string", "PagedKVError"]
+           "pa_set_decode_kernel", "pa_get_device_error", "pa_status_string", "PagedKVError"]
 
 
 def _stream(stream):
@@ -126,6 +126,14 @@ def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, par
                                 block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, Hkv, D, b,
                                 float(scale), int(partition_tokens), _dtype_id(k_pool), _stream(stream)),
           "pa_decode_noalloc")
+
+
+DECODE_KERNELS = {"auto": 0, "simt": 1, "mma": 2}
+
+
+def pa_set_decode_kernel(kernel: str) -> None:
+    """Process-wide choice of the decode kernel: "auto", "simt" or "mma"."""
+    check(load().pa_set_decode_kernel(DECODE_KERNELS[kernel]), "pa_set_decode_kernel")
 
 
 def pa_get_device_error(stream=None) -> int:

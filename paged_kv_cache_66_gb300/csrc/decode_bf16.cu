@@ -1,6 +1,6 @@
 // Instantiations of the paged decode kernels for __nv_bfloat16 pools (one translation
 // unit per dtype so the build compiles them in parallel).
-#include "decode_simt.cuh"
+#include "decode_dispatch.cuh"
 
 namespace pa {
 

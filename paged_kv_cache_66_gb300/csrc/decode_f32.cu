@@ -1,6 +1,6 @@
 // Instantiations of the paged decode kernels for float pools (one translation
 // unit per dtype so the build compiles them in parallel).
-#include "decode_simt.cuh"
+#include "decode_dispatch.cuh"
 
 namespace pa {
 

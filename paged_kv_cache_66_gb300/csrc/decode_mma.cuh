@@ -1,0 +1,403 @@
+// Paged decode attention with the GQA q-group x 16-token tile on the tensor
+// cores (mma.sync m16n8k16, fp32 accumulate), for fp16 and bf16 pools.
+//
+// Computes the same partition (max, normaliser, output) as the CUDA-core
+// kernel -- online softmax over the blocks of one partition for all G query
+// heads of one KV head ("25. Paged attention and prefix caching", "Attention
+// that reads through the table"; "Chapter 7 Paged KV Cache and Memory
+// Management", 4.2) -- and hands it to the same merge.
+//
+// Why the tensor cores: the CUDA-core kernel needs ~79 instructions per
+// (token, KV head) and is issue-bound well below the HBM roofline.  Here one
+// 16-token tile costs D/16 MMAs for the scores and D/16 for the output:
+//   S^T[16 tok x 8 heads] = K_tile[16 x D] . Q^T[D x 8]      (A = K from smem, B = Q in registers)
+//   O^T[D x 8 heads]     += V_tile^T[D x 16] . P^T[16 x 8]    (A = V^T from smem, B = P^T)
+// The query group (G <= 8) sits on the N = 8 side; unused columns are zero.
+// The score fragment becomes the P^T operand with one movmatrix transpose per
+// 8 tokens, so P never touches shared memory.
+//
+// Data movement: each 16-token K (and V) tile of one (block, KV head) is
+// fetched by TMA as D/64 boxes of 16 rows x 128 bytes with the 128-byte
+// swizzle, so the ldmatrix reads of the fragments are bank-conflict free.
+// Each warp owns every NW-th tile of the partition and a STAGES-deep ring,
+// lane 0 issuing the tensor copies STAGES tiles ahead on per-stage mbarriers.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode_merge.cuh"
+#include "pa_common.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <typename T>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__half>(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------------ configuration
+template <typename T, int D, int G>
+struct MmaCfg {
+    static_assert(sizeof(T) == 2, "tensor-core path is for 16-bit pools");
+    static constexpr int TILE = 16;                    // tokens per tile (M of the score MMA)
+    static constexpr int NBOX = D / 64;                // 128-byte boxes per 16-token row block
+    static constexpr int BOX_BYTES = TILE * 128;       // 2 KiB, 1024-byte aligned in smem
+    static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
+    static constexpr int NW = 4;
+    static constexpr int ST_RAW = (96 * 1024) / (NW * STAGE_BYTES);
+    static constexpr int STAGES = ST_RAW < 2 ? 2 : (ST_RAW > 4 ? 4 : ST_RAW);
+    static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = RING_BYTES;
+    static constexpr int TBL_OFF = BAR_OFF + NW * STAGES * 8;
+    static constexpr int KSTEPS = D / 16;
+    static constexpr int RED_BYTES = NW * G * (D + 2) * 4;
+    static_assert(RED_BYTES <= RING_BYTES, "merge scratch aliases the ring");
+    static_assert(G >= 1 && G <= 8, "query group on the N = 8 side");
+    // + 1 KiB so the ring can be aligned to 1024 bytes for the 128-byte swizzle
+    static constexpr size_t smem_bytes(int table_entries) {
+        return 1024 + static_cast<size_t>(TBL_OFF) + static_cast<size_t>(table_entries) * 4;
+    }
+};
+
+// Byte offset of (token row r, 16-byte chunk c) of a tile stored as NBOX boxes
+// of 16 rows x 128 bytes with the 128-byte swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
+    decode_partition_mma(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap) {
+    using C = MmaCfg<T, D, G>;
+    constexpr int NW = C::NW, STAGES = C::STAGES, KSTEPS = C::KSTEPS;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem =
+        smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-byte aligned ring
+
+    const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bs = p.block_size, P = p.partition_tokens;
+    const int cap = p.max_blocks * bs;
+    int L = __ldg(p.seq_lens + s);
+    if (L < 0 || L > cap) {
+        if (part == 0 && kvh == 0 && tid == 0) flag_error(p.err, PA_DEVERR_SEQLEN);
+        L = L < 0 ? 0 : cap;
+    }
+    const int n_parts = (L + P - 1) / P;
+    T* out_rows = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + kvh * G) * D;
+    if (L == 0) {
+        if (part == 0)
+            for (int i = tid; i < G * D; i += blockDim.x) out_rows[i] = Elt<T>::from_f32(0.f);
+        return;
+    }
+    const int tok0 = part * P;
+    if (tok0 >= L) return;
+    const int tok1 = min(L, tok0 + P);
+    const int n_tiles = (tok1 - tok0 + C::TILE - 1) / C::TILE;
+
+    int* tbl = reinterpret_cast<int*>(smem + C::TBL_OFF);
+    const int nblk = (tok1 - tok0 + bs - 1) / bs;
+    const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks + tok0 / bs;
+    for (int i = tid; i < nblk; i += blockDim.x) {
+        int e = __ldg(trow + i);
+        if (e < 0 || e >= p.num_blocks) {
+            flag_error(p.err, PA_DEVERR_TABLE);
+            e = -1;
+        }
+        tbl[i] = e;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * STAGES;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    unsigned char* ring = smem + warp * STAGES * C::STAGE_BYTES;
+    const int my_n = warp < n_tiles ? (n_tiles - warp + NW - 1) / NW : 0;
+
+    auto issue = [&](int j) {
+        const int i = warp + j * NW;
+        const int st = j % STAGES;
+        const int blk = tbl[(i * C::TILE) / bs];
+        if (blk < 0) {
+            mbar_arrive_expect_tx(&bars[st], 0);
+            return;
+        }
+        const int row = (blk * p.hkv + kvh) * bs + (i * C::TILE) % bs;
+        unsigned char* dst = ring + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&bars[st], 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < C::NBOX; ++bx) {
+            tma_load_2d(dst + bx * C::BOX_BYTES, &kmap, bx * 64, row, &bars[st]);
+            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &vmap, bx * 64, row, &bars[st]);
+        }
+    };
+    if (lane == 0)
+        for (int j = 0; j < STAGES && j < my_n; ++j) issue(j);
+
+    // ---- query fragments (B operand of the score MMA): lane (g, t) holds
+    // Q[head g][k0 + 2t, +1] and Q[head g][k0 + 8 + 2t, +1]; heads >= G are zero.
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t qb[KSTEPS][2];
+    {
+        const T* qrow = static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.hq + kvh * G + g) * D;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+            if (g < G) {
+                qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 2 * t));
+                qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + 2 * t));
+            } else {
+                qb[ks][0] = 0u;
+                qb[ks][1] = 0u;
+            }
+        }
+    }
+    // ---- output accumulators O^T: acc[mt] = {O[h0][dim mt*16+g], O[h1][..], O[h0][dim mt*16+g+8], O[h1][..]}
+    // with h0 = 2t, h1 = 2t + 1
+    float acc[KSTEPS][4];
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const float sl2 = p.scale_log2;
+
+    // ldmatrix addressing: lane provides row (lane & 7) of matrix (lane >> 3)
+    const int lm = lane >> 3, lr = lane & 7;
+
+    for (int j = 0; j < my_n; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait_bounded(&bars[st], (j / STAGES) & 1)) {
+            if (lane == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
+            for (int r = j + 1; r < my_n && r < j + STAGES; ++r) mbar_wait_bounded(&bars[r % STAGES], (r / STAGES) & 1);
+            break;
+        }
+        const int i = warp + j * NW;
+        const int nv = min(C::TILE, tok1 - (tok0 + i * C::TILE));
+        const bool present = tbl[(i * C::TILE) / bs] >= 0;
+        unsigned char* kt = ring + st * C::STAGE_BYTES;
+        unsigned char* vt = kt + C::TILE_BYTES;
+        if (present) {
+            // ---- scores S^T = K Q^T (16 tokens x 8 heads)
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kbase = smem_u32(kt);
+            const int krow = lr + (lm & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(kbase + swz(krow, ks * 2 + (lm >> 1)), a);
+                mma16816<T>(sc, a, qb[ks][0], qb[ks][1]);
+            }
+            // sc = {S[tok g][h0], S[tok g][h1], S[tok g+8][h0], S[tok g+8][h1]}
+            const bool v0 = g < nv, v1 = g + 8 < nv;
+            sc[0] = v0 ? sc[0] * sl2 : -INFINITY;
+            sc[1] = v0 ? sc[1] * sl2 : -INFINITY;
+            sc[2] = v1 ? sc[2] * sl2 : -INFINITY;
+            sc[3] = v1 ? sc[3] * sl2 : -INFINITY;
+            float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            if (mx0 > m0 + kLazyRescale) {
+                const float a0 = exp2f(m0 - mx0);
+                l0 *= a0;
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    acc[mt][0] *= a0;
+                    acc[mt][2] *= a0;
+                }
+                m0 = mx0;
+            }
+            if (mx1 > m1 + kLazyRescale) {
+                const float a1 = exp2f(m1 - mx1);
+                l1 *= a1;
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    acc[mt][1] *= a1;
+                    acc[mt][3] *= a1;
+                }
+                m1 = mx1;
+            }
+            const float p0 = exp2f(sc[0] - m0), p1 = exp2f(sc[1] - m1);
+            const float p2 = exp2f(sc[2] - m0), p3 = exp2f(sc[3] - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            // P^T operand: transpose the 8x8 (token x head) halves
+            const uint32_t pb0 = movmatrix_t(pack2<T>(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack2<T>(p2, p3));
+            if (nv < C::TILE) {
+                // unwritten slots of the tail may hold anything (NaN * 0 = NaN): zero those V rows
+                for (int e = lane; e < (C::TILE - nv) * (D / 8); e += 32) {
+                    const int r = nv + e / (D / 8), c = e % (D / 8);
+                    *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            // ---- O^T += V^T P^T
+            const uint32_t vbase = smem_u32(vt);
+            const int vrow = lr + (lm >> 1) * 8;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_t(vbase + swz(vrow, mt * 2 + (lm & 1)), a);
+                mma16816<T>(acc[mt], a, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && j + STAGES < my_n) {
+            fence_proxy_async_smem();  // order this warp's shared accesses before the next async copy
+            issue(j + STAGES);
+        }
+    }
+
+    // ---- normalisers: sum over the 8 token rows held by lanes with the same t
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+
+    // ---- merge the warps through shared memory (aliases the ring)
+    __syncthreads();
+    float* red_m = reinterpret_cast<float*>(smem);
+    float* red_l = red_m + NW * G;
+    float* red_acc = red_l + NW * G;
+    const int h0 = 2 * t, h1 = 2 * t + 1;
+    if (g == 0) {
+        if (h0 < G) {
+            red_m[warp * G + h0] = m0;
+            red_l[warp * G + h0] = l0;
+        }
+        if (h1 < G) {
+            red_m[warp * G + h1] = m1;
+            red_l[warp * G + h1] = l1;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+        const int d0 = mt * 16 + g;
+        if (h0 < G) {
+            red_acc[(warp * G + h0) * D + d0] = acc[mt][0];
+            red_acc[(warp * G + h0) * D + d0 + 8] = acc[mt][2];
+        }
+        if (h1 < G) {
+            red_acc[(warp * G + h1) * D + d0] = acc[mt][1];
+            red_acc[(warp * G + h1) * D + d0 + 8] = acc[mt][3];
+        }
+    }
+    __syncthreads();
+
+    const bool direct = n_parts == 1;
+    for (int idx = tid; idx < G * D; idx += blockDim.x) {
+        const int hh = idx / D, d = idx - hh * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + hh]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = exp2f(red_m[w * G + hh] - M);
+                num = fmaf(f, red_acc[(w * G + hh) * D + d], num);
+                den = fmaf(f, red_l[w * G + hh], den);
+            }
+        }
+        if (direct) {
+            out_rows[idx] = Elt<T>::from_f32(den > 0.f ? num / den : 0.f);
+        } else {
+            const size_t row = (static_cast<size_t>(s) * p.hq + kvh * G + hh) * p.max_partitions + part;
+            p.ws_acc[row * D + d] = num;
+            if (d == 0) {
+                p.ws_ml[row * 2] = M;
+                p.ws_ml[row * 2 + 1] = den;
+            }
+        }
+    }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       cudaStream_t stream) {
+    using C = MmaCfg<T, D, G>;
+    const size_t smem = C::smem_bytes(p.partition_tokens / p.block_size);
+    static int configured_for = -1;  // device on which the attribute was last set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+        cudaError_t e = cudaFuncSetAttribute(decode_partition_mma<T, D, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(C::smem_bytes(8192 / 16)));
+        if (e != cudaSuccess) return e;
+        configured_for = dev;
+    }
+    dim3 grid(p.max_partitions, p.hkv, p.batch);
+    decode_partition_mma<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p, kmap, vmap);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.max_partitions <= 1) return e;
+    return launch_merge<T, D>(p, stream);
+}
+
+}  // namespace pa

@@ -28,6 +28,7 @@
 //  * warps merge their states through shared memory at the end.
 #pragma once
 
+#include "decode_merge.cuh"
 #include "pa_common.cuh"
 #include "pa_launch.h"
 
@@ -59,8 +60,6 @@ struct SimtCfg {
         return static_cast<size_t>(TBL_OFF) + static_cast<size_t>(table_entries) * 4;
     }
 };
-
-constexpr float kLazyRescale = 8.0f;  // log2 units
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(SimtCfg<T, D, G>::NW * 32)
@@ -311,34 +310,6 @@ __global__ void __launch_bounds__(SimtCfg<T, D, G>::NW * 32)
     }
 }
 
-// Merge of the partitions of one (sequence, query head): "Chapter 7 Paged KV
-// Cache and Memory Management", 4.2 -- new reference max, rescale every
-// partial onto it, add, divide.  Partitions with normaliser 0 contribute 0.
-template <typename T, int D>
-__global__ void __launch_bounds__(D) decode_merge(const DecodeParams p) {
-    const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
-    const int cap = p.max_blocks * p.block_size;
-    int L = __ldg(p.seq_lens + s);
-    L = L < 0 ? 0 : (L > cap ? cap : L);
-    const int n_parts = (L + p.partition_tokens - 1) / p.partition_tokens;
-    if (n_parts <= 1) return;
-    const size_t row0 = (static_cast<size_t>(s) * p.hq + h) * p.max_partitions;
-    const float* ml = p.ws_ml + row0 * 2;
-    float M = -INFINITY;
-    for (int i = 0; i < n_parts; ++i) M = fmaxf(M, ml[2 * i]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-        const float* acc = p.ws_acc + row0 * D + d;
-        for (int i = 0; i < n_parts; ++i) {
-            const float f = exp2f(ml[2 * i] - M);
-            num = fmaf(f, acc[static_cast<size_t>(i) * D], num);
-            den = fmaf(f, ml[2 * i + 1], den);
-        }
-    }
-    T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + h) * D;
-    out[d] = Elt<T>::from_f32(den > 0.f ? num / den : 0.f);
-}
-
 template <typename T, int D, int G>
 cudaError_t launch_simt(const DecodeParams& p, cudaStream_t stream) {
     using C = SimtCfg<T, D, G>;
@@ -358,29 +329,7 @@ cudaError_t launch_simt(const DecodeParams& p, cudaStream_t stream) {
     decode_partition_simt<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.max_partitions <= 1) return e;
-    decode_merge<T, D><<<dim3(p.hq, p.batch), D, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-template <typename T, int D>
-cudaError_t dispatch_group(const DecodeParams& p, cudaStream_t stream) {
-    switch (p.hq / p.hkv) {
-        case 1: return launch_simt<T, D, 1>(p, stream);
-        case 2: return launch_simt<T, D, 2>(p, stream);
-        case 4: return launch_simt<T, D, 4>(p, stream);
-        case 8: return launch_simt<T, D, 8>(p, stream);
-        default: return cudaErrorNotSupported;
-    }
-}
-
-template <typename T>
-cudaError_t dispatch_decode(const DecodeParams& p, cudaStream_t stream) {
-    switch (p.d) {
-        case 64: return dispatch_group<T, 64>(p, stream);
-        case 128: return dispatch_group<T, 128>(p, stream);
-        case 256: return dispatch_group<T, 256>(p, stream);
-        default: return cudaErrorNotSupported;
-    }
+    return launch_merge<T, D>(p, stream);
 }
 
 }  // namespace pa

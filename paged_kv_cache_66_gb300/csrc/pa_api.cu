@@ -1,9 +1,12 @@
 // C ABI of the paged KV-cache device library: argument validation, the
 // device error word, and dispatch to the kernels.  See include/pagedkv.h for
 // the contract of every entry point.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "pa_common.cuh"
 #include "pa_launch.h"
@@ -31,6 +34,11 @@ int* error_word() {
     }
     return g_err_ptr[dev];
 }
+
+std::atomic<int> g_decode_kernel{PA_DECODE_AUTO};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
 
 inline bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -71,7 +79,36 @@ WsLayout ws_layout(int batch, int hq, int d, int max_blocks, int b, int part) {
 
 }  // namespace
 
+namespace pa {
+
+bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace pa
+
 extern "C" {
+
+pa_status pa_set_decode_kernel(pa_decode_kernel kernel) {
+    if (kernel != PA_DECODE_AUTO && kernel != PA_DECODE_SIMT && kernel != PA_DECODE_MMA) return PA_ERR_INVALID;
+    g_decode_kernel.store(kernel);
+    return PA_OK;
+}
 
 pa_status pa_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slot_mapping,
                        int64_t num_tokens, int64_t num_blocks, int num_kv_heads, int head_dim, int block_size,
@@ -169,6 +206,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
     p.partition_tokens = part;
     p.max_partitions = ws.partitions < 1 ? 1 : ws.partitions;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.kernel = g_decode_kernel.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
         case PA_F32: return from_cuda(pa::launch_decode_f32(p, st));

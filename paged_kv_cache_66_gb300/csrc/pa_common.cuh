@@ -139,6 +139,8 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// Online softmax keeps a stale reference max until a tile's max exceeds it by
+// more than this many log2 units (exponents stay <= 2^8; exact after O / l).
+constexpr float kLazyRescale = 8.0f;
 
 }  // namespace pa

@@ -1,6 +1,7 @@
 // Internal launcher interface between the C ABI (pa_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,7 +34,12 @@ struct DecodeParams {
     int partition_tokens;
     int max_partitions;         // P = ceil(max_blocks * b / partition_tokens)
     float scale_log2;           // scale * log2(e)
+    int kernel;                 // pa_decode_kernel choice (PA_DECODE_AUTO / _SIMT / _MMA)
 };
+
+// 2-D TMA descriptor of a pool viewed as [rows, D] 16-bit elements, boxes of
+// 16 rows x 64 elements (128 bytes) with the 128-byte swizzle.
+bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d);
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slots,
                              int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,

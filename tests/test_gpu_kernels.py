@@ -28,6 +28,14 @@ def api():
     return _api
 
 
+@pytest.fixture(params=["simt", "mma"])
+def kernel(request, api):
+    """Run a decode test once per partition kernel (CUDA cores / tensor cores)."""
+    api.pa_set_decode_kernel(request.param)
+    yield request.param
+    api.pa_set_decode_kernel("auto")
+
+
 def _rand(shape, dtype, gen):
     return torch.randn(shape, generator=gen, dtype=torch.float32).to(dtype)
 
@@ -150,8 +158,10 @@ CASES = [
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("case", CASES)
-def test_decode_matches_oracle(api, dtype, case):
+def test_decode_matches_oracle(api, kernel, dtype, case):
     Hq, Hkv, D, b, lengths, part = case
+    if kernel == "mma" and dtype == torch.float32:
+        pytest.skip("tensor-core kernel is for 16-bit pools (covered by the unsupported test)")
     gen = torch.Generator().manual_seed(hash((Hq, Hkv, D, b, len(lengths), part)) & 0xFFFF)
     t, K, V, tables, lens = _setup_paged(lengths, Hkv, D, b, dtype, gen)
     q = _rand((len(lengths), Hq, D), dtype, gen)
@@ -163,8 +173,37 @@ def test_decode_matches_oracle(api, dtype, case):
     assert api.pa_get_device_error() == 0
 
 
+def test_mma_kernel_rejects_fp32(api):
+    gen = torch.Generator().manual_seed(9)
+    t, K, V, tables, lens = _setup_paged([5], 2, 64, 16, torch.float32, gen)
+    q = _rand((1, 4, 64), torch.float32, gen)
+    api.pa_set_decode_kernel("mma")
+    try:
+        with pytest.raises(api.PagedKVError) as e:
+            _run_decode(api, q, K, V, tables, lens, 0.125)
+        assert e.value.status == 2                      # PA_ERR_UNSUPPORTED
+    finally:
+        api.pa_set_decode_kernel("auto")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_simt_and_mma_kernels_agree(api, dtype):
+    gen = torch.Generator().manual_seed(10)
+    lengths = [1, 17, 700, 2500]
+    t, K, V, tables, lens = _setup_paged(lengths, 8, 128, 16, dtype, gen)
+    q = _rand((4, 32, 128), dtype, gen)
+    outs = {}
+    for k in ("simt", "mma"):
+        api.pa_set_decode_kernel(k)
+        outs[k] = _run_decode(api, q, K, V, tables, lens, 0.088).double()
+    api.pa_set_decode_kernel("auto")
+    assert (outs["simt"] - outs["mma"]).abs().max().item() <= TOL[dtype]
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_decode_length_one_is_v0_exactly(api, dtype):
+def test_decode_length_one_is_v0_exactly(api, kernel, dtype):
+    if kernel == "mma" and dtype == torch.float32:
+        pytest.skip("tensor-core kernel is for 16-bit pools")
     gen = torch.Generator().manual_seed(1)
     t, K, V, tables, lens = _setup_paged([1, 1, 1], 2, 128, 16, dtype, gen)
     q = _rand((3, 8, 128), dtype, gen)
@@ -175,7 +214,7 @@ def test_decode_length_one_is_v0_exactly(api, dtype):
             assert torch.equal(got[s, h], V[blk, h // 4, 0])
 
 
-def test_decode_zero_length_writes_zeros(api):
+def test_decode_zero_length_writes_zeros(api, kernel):
     gen = torch.Generator().manual_seed(2)
     t, K, V, tables, lens = _setup_paged([5, 40], 2, 64, 16, torch.float16, gen)
     lens[0] = 0
@@ -186,7 +225,7 @@ def test_decode_zero_length_writes_zeros(api):
     assert np.abs(got[1:].double().numpy() - want).max() <= 2e-3
 
 
-def test_decode_partition_size_does_not_matter(api):
+def test_decode_partition_size_does_not_matter(api, kernel):
     gen = torch.Generator().manual_seed(4)
     lengths = [3000, 129, 4096, 1]
     t, K, V, tables, lens = _setup_paged(lengths, 8, 128, 16, torch.float16, gen)
@@ -196,7 +235,7 @@ def test_decode_partition_size_does_not_matter(api):
         assert (o - outs[0]).abs().max().item() <= 2e-3
 
 
-def test_decode_physical_placement_is_invisible(api):
+def test_decode_physical_placement_is_invisible(api, kernel):
     """Same logical history at two different physical placements: identical bits."""
     gen = torch.Generator().manual_seed(5)
     lengths = [777, 40]
@@ -211,7 +250,7 @@ def test_decode_physical_placement_is_invisible(api):
     assert torch.equal(a, c)
 
 
-def test_decode_unwritten_slots_are_masked(api):
+def test_decode_unwritten_slots_are_masked(api, kernel):
     """NaN garbage past the length in the tail block must not leak into the output."""
     gen = torch.Generator().manual_seed(6)
     t, K, V, tables, lens = _setup_paged([21], 2, 64, 16, torch.float16, gen)
@@ -225,7 +264,7 @@ def test_decode_unwritten_slots_are_masked(api):
     assert np.abs(got.double().numpy() - want).max() <= 2e-3
 
 
-def test_decode_bad_table_entry_is_flagged_not_faulted(api):
+def test_decode_bad_table_entry_is_flagged_not_faulted(api, kernel):
     gen = torch.Generator().manual_seed(7)
     t, K, V, tables, lens = _setup_paged([40, 40], 2, 64, 16, torch.float16, gen)
     tables[1, 1] = 10_000                           # outside the pool
