@@ -50,7 +50,7 @@ def up_to_date() -> bool:
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     if src.endswith(".cu"):
-        cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *os.environ.get("PA_NVCC_EXTRA", "").split(), "-c", src, "-o", obj]
         if verbose_ptxas:
             cmd[1:1] = ["-Xptxas", "-v"]
     else:

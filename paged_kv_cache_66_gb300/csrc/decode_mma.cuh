@@ -103,9 +103,17 @@ struct MmaCfg {
     static constexpr int BOX_BYTES = TILE * 128;       // 2 KiB, 1024-byte aligned in smem
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
+#ifdef PA_MMA_WARPS
+    static constexpr int NW = PA_MMA_WARPS;  // build-time override (tuning sweeps)
+#else
     static constexpr int NW = 4;
+#endif
     static constexpr int ST_RAW = (96 * 1024) / (NW * STAGE_BYTES);
+#ifdef PA_MMA_STAGES
+    static constexpr int STAGES = PA_MMA_STAGES;
+#else
     static constexpr int STAGES = ST_RAW < 2 ? 2 : (ST_RAW > 4 ? 4 : ST_RAW);
+#endif
     static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_BYTES;
     static constexpr int TBL_OFF = BAR_OFF + NW * STAGES * 8;
