@@ -103,16 +103,18 @@ struct MmaCfg {
     static constexpr int BOX_BYTES = TILE * 128;       // 2 KiB, 1024-byte aligned in smem
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
+    // 2 stages x 4 warps (2 warps for D = 256): 32-64 KiB per CTA, so 3+ CTAs
+    // share an SM; deeper rings measured slower on the long-context workload
+    // (fewer resident CTAs to cover each CTA's start and end).
 #ifdef PA_MMA_WARPS
     static constexpr int NW = PA_MMA_WARPS;  // build-time override (tuning sweeps)
 #else
-    static constexpr int NW = 4;
+    static constexpr int NW = STAGE_BYTES >= 16384 ? 2 : 4;
 #endif
-    static constexpr int ST_RAW = (96 * 1024) / (NW * STAGE_BYTES);
 #ifdef PA_MMA_STAGES
     static constexpr int STAGES = PA_MMA_STAGES;
 #else
-    static constexpr int STAGES = ST_RAW < 2 ? 2 : (ST_RAW > 4 ? 4 : ST_RAW);
+    static constexpr int STAGES = 2;
 #endif
     static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_BYTES;
@@ -120,6 +122,7 @@ struct MmaCfg {
     static constexpr int KSTEPS = D / 16;
     static constexpr int RED_BYTES = NW * G * (D + 2) * 4;
     static_assert(RED_BYTES <= RING_BYTES, "merge scratch aliases the ring");
+    static_assert((2 + 2 * kMergeChunk) * G * 4 <= RING_BYTES, "fused merge scratch aliases the ring");
     static_assert(G >= 1 && G <= 8, "query group on the N = 8 side");
     // + 1 KiB so the ring can be aligned to 1024 bytes for the 128-byte swizzle
     static constexpr size_t smem_bytes(int table_entries) {
@@ -384,6 +387,8 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
             }
         }
     }
+    if (!direct) merge_if_last<T, D, G>(p, s, kvh, n_parts, reinterpret_cast<float*>(smem), tid, blockDim.x);
+
 }
 
 template <typename T, int D, int G>
@@ -403,9 +408,7 @@ cudaError_t launch_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUt
     }
     dim3 grid(p.max_partitions, p.hkv, p.batch);
     decode_partition_mma<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p, kmap, vmap);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || p.max_partitions <= 1) return e;
-    return launch_merge<T, D>(p, stream);
+    return cudaGetLastError();
 }
 
 }  // namespace pa
