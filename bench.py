@@ -347,7 +347,13 @@ def run_ours(args, ws, rank, local):
 
 
 def run_e2e(args, wl, rp, dev, ws):
-    """K steps through the public API with host buffers (pinned), copies timed."""
+    """K steps through the public API with host buffers (pinned), copies timed.
+
+    Per step: the C++ plan writes slots / lengths / tables into one pinned
+    metadata buffer (one host->device copy); the step's q, new K and new V rows
+    of every layer sit in one pinned buffer (one host->device copy); every
+    layer's output lands in one device buffer read back with one copy.
+    """
     from paged_kv_cache_66_gb300 import api
     from workload import configs as wc
     # inputs of the next K steps, created on the host (not timed): positions
@@ -355,29 +361,35 @@ def run_e2e(args, wl, rp, dev, ws):
     uids = list(wl.step_ops[rp.steps_done][-1][1])
     base = np.array([rp.host.length(u) for u in uids], dtype=np.int64)
     B, nL = len(uids), len(rp.layers)
+    nq, nk = B * wl.Hq * wl.D, B * wl.Hkv * wl.D
+    row = nq + 2 * nk
     host_in = []
     for j in range(args.steps):
         pos = base + j
         owners = np.array([wl.content_owner(u, int(p)) for u, p in zip(uids, pos)])
-        qs, ks, vs = [], [], []
-        for layer in rp.layers:
-            qs.append(wc.q_rows(wl, layer, rp.steps_done + j, np.arange(B)).pin_memory())
-            ks.append(wc.kv_rows(wl, layer, "k", owners, pos).pin_memory())
-            vs.append(wc.kv_rows(wl, layer, "v", owners, pos).pin_memory())
-        host_in.append((qs, ks, vs))
-    out_host = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype).pin_memory() for _ in range(nL)]
+        x = torch.empty((nL, row), dtype=wl.torch_dtype)
+        for li, layer in enumerate(rp.layers):
+            x[li, :nq] = wc.q_rows(wl, layer, rp.steps_done + j, np.arange(B)).reshape(-1)
+            x[li, nq:nq + nk] = wc.kv_rows(wl, layer, "k", owners, pos).reshape(-1)
+            x[li, nq + nk:] = wc.kv_rows(wl, layer, "v", owners, pos).reshape(-1)
+        host_in.append(x.pin_memory())
     stride = max(len(rp.host.table(u)) for u in uids) + args.steps // wl.b + 2
-    # two sets of pinned metadata buffers, reused every other step once their upload is done
-    bufs = [{"tables": torch.zeros((B, stride), dtype=torch.int32).pin_memory(),
-             "lens": torch.zeros(B, dtype=torch.int32).pin_memory(),
-             "slots": torch.zeros(B, dtype=torch.int64).pin_memory(), "ev": None} for _ in range(2)]
-    d_q = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev) for _ in range(nL)]
-    d_k = [torch.empty((B, wl.Hkv, wl.D), dtype=wl.torch_dtype, device=dev) for _ in range(nL)]
-    d_v = [torch.empty_like(x) for x in d_k]
-    d_out = [torch.empty_like(x) for x in d_q]
-    d_tables = torch.empty((B, stride), dtype=torch.int32, device=dev)
-    d_lens = torch.empty(B, dtype=torch.int32, device=dev)
-    d_slots = torch.empty(B, dtype=torch.int64, device=dev)
+    meta_bytes = B * 8 + B * 4 + B * stride * 4
+
+    def meta_views(buf):
+        return (buf[:B * 8].view(torch.int64), buf[B * 8:B * 12].view(torch.int32),
+                buf[B * 12:].view(torch.int32).view(B, stride))
+
+    # two pinned metadata buffers, reused every other step once their upload is done
+    bufs = [{"meta": torch.zeros(meta_bytes, dtype=torch.uint8).pin_memory(), "ev": None} for _ in range(2)]
+    d_meta = torch.empty(meta_bytes, dtype=torch.uint8, device=dev)
+    d_slots, d_lens, d_tables = meta_views(d_meta)
+    d_x = torch.empty((nL, row), dtype=wl.torch_dtype, device=dev)
+    d_q = [d_x[li, :nq].view(B, wl.Hq, wl.D) for li in range(nL)]
+    d_k = [d_x[li, nq:nq + nk].view(B, wl.Hkv, wl.D) for li in range(nL)]
+    d_v = [d_x[li, nq + nk:].view(B, wl.Hkv, wl.D) for li in range(nL)]
+    d_out = torch.empty((nL, B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev)
+    out_host = torch.empty_like(d_out, device="cpu").pin_memory()
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     _barrier(ws)
@@ -390,32 +402,27 @@ def run_e2e(args, wl, rp, dev, ws):
         buf = bufs[j % 2]
         if buf["ev"] is not None:
             buf["ev"].synchronize()
-        tables, lens, slots = buf["tables"], buf["lens"], buf["slots"]
-        tn, ln, sn = tables.numpy(), lens.numpy(), slots.numpy()
-        pairs, width = rp.host.decode_step(uids, tn, ln, sn)
+        slots, lens, tables = meta_views(buf["meta"])
+        ln = lens.numpy()
+        pairs, width = rp.host.decode_step(uids, tables.numpy(), ln, slots.numpy())
         kv += _kv_bytes(wl, ln) * nL
-        d_tables.copy_(tables, non_blocking=True)
-        d_lens.copy_(lens, non_blocking=True)
-        d_slots.copy_(slots, non_blocking=True)
+        d_meta.copy_(buf["meta"], non_blocking=True)
         buf["ev"] = torch.cuda.Event()
         buf["ev"].record(stream)
-        h2d += tables.numel() * 4 + lens.numel() * 4 + slots.numel() * 8
+        h2d += meta_bytes
         if len(pairs):
             d_pairs = torch.as_tensor(pairs).to(dev, non_blocking=False)
             api.pa_copy_blocks(rp.k_pools, rp.v_pools, d_pairs)
             h2d += pairs.nbytes
-        qs, ks, vs = host_in[j]
+        d_x.copy_(host_in[j], non_blocking=True)
+        h2d += host_in[j].numel() * wl.elt
         wsbuf = rp.workspace_for(B, stride)
         for li in range(nL):
-            d_q[li].copy_(qs[li], non_blocking=True)
-            d_k[li].copy_(ks[li], non_blocking=True)
-            d_v[li].copy_(vs[li], non_blocking=True)
-            h2d += (qs[li].numel() + ks[li].numel() + vs[li].numel()) * wl.elt
             api.pa_kv_append(d_k[li], d_v[li], rp.k_pools[li], rp.v_pools[li], d_slots)
             api.pa_decode(d_out[li], d_q[li], rp.k_pools[li], rp.v_pools[li], d_tables, d_lens, wl.scale,
                           partition_tokens=rp.partition_tokens, workspace=wsbuf if wsbuf.numel() else None)
-            out_host[li].copy_(d_out[li], non_blocking=True)
-            d2h += d_out[li].numel() * wl.elt
+        out_host.copy_(d_out, non_blocking=True)
+        d2h += d_out.numel() * wl.elt
     t1.record(stream)
     torch.cuda.synchronize()
     rp.steps_done += args.steps

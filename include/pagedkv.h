@@ -107,14 +107,13 @@ pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int num_lay
                          size_t block_bytes, void* stream);
 
 /*
- * pa_decode_workspace_size -- bytes of scratch pa_decode needs for a batch
- * of B sequences with Hq query heads whose block tables have `max_blocks`
- * columns: one 32-bit counter per (sequence, query head), and per (sequence,
- * query head, partition) one fp32 running max, one fp32 normaliser and D
- * fp32 partial output values.  Returns 0 when every sequence fits one
- * partition (max_blocks * b <= partition tokens).  partition_tokens = 0
- * selects the default (512).  The contents need no initialisation: pa_decode
- * zeroes the counters itself, on `stream`, before it launches the kernel.
+ * pa_decode_workspace_size -- bytes of fp32 scratch pa_decode needs for a
+ * batch of B sequences with Hq query heads whose block tables have
+ * `max_blocks` columns: per (sequence, query head, partition) one running
+ * max, one normaliser and D partial output values.  Returns 0 when every
+ * sequence fits one partition (max_blocks * b <= partition tokens).
+ * partition_tokens = 0 selects the default (512).  The contents need no
+ * initialisation.
  */
 size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int max_blocks,
                                 int block_size, int partition_tokens);
@@ -136,9 +135,7 @@ size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int ma
  *   t < L_s with fp32 accumulation, rounded once to `dtype`.
  *   Sequences longer than `partition_tokens` (0 = 512; a multiple of 16 and
  *   of b) are split into partitions whose (max, normaliser, partial output)
- *   go to `workspace`; the last partition of each (sequence, KV head) to
- *   finish merges them (a counter in the workspace, zeroed by this call with
- *   an asynchronous memset on `stream` before the kernel).
+ *   go to `workspace` and are merged by a second kernel.
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
  *                 bytes, 16-byte aligned; may be NULL when that size is 0.
  *   Supported: D in {64, 128, 256}; Hq / Hkv in {1, 2, 4, 8}; b a multiple of

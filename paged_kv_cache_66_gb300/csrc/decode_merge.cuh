@@ -3,6 +3,14 @@
 // take the largest partition max as the new reference, rescale every
 // partition's normaliser and partial output onto it, add, divide.  A partition
 // with normaliser 0 (nothing valid) contributes nothing.
+//
+// One CTA of 128 threads per (query head, sequence).  The partition weights
+// exp2(m_p - M) go to shared memory once; then the CTA's threads form
+// 128 / (D/4) "streams" of D/4 lanes, each lane owning 4 output dimensions,
+// and stream k walks partitions k, k + streams, ... with 8 float4 loads in
+// flight per lane.  Streams are combined in a fixed order, so the result is
+// deterministic.  (A variant fused into the partition kernel -- the last CTA
+// of a group merging -- measured slower: its merge sat on the kernel's tail.)
 #pragma once
 
 #include "pa_common.cuh"
@@ -10,101 +18,122 @@
 
 namespace pa {
 
-constexpr int kMergeChunk = 256;  // partitions per shared-memory chunk
+constexpr int kMergeThreads = 128;
+constexpr int kMergeChunk = 1024;  // partitions whose weights sit in shared memory at once
 
-// Fused merge: every partition CTA of one (sequence, KV head) group bumps a
-// counter after publishing its partials; the CTA that arrives last merges the
-// group's G heads.  pa_decode zeroes the counters before the partition kernel.
-//   nthreads threads (>= 64); `sm` = shared scratch of at least
-//   (2 + 2 * kMergeChunk) * G floats.  The reduction order is fixed, so the
-//   result does not depend on which CTA merges or on timing.
-template <typename T, int D, int G>
-__device__ __forceinline__ void merge_if_last(const DecodeParams& p, int s, int kvh, int n_parts, float* sm,
-                                              int tid, int nthreads) {
-    __shared__ int s_last;
-    __threadfence();  // this CTA's partials are visible device-wide before it is counted
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge(const DecodeParams p) {
+    constexpr int LPS = D / 4;                       // lanes per stream (4 dims each)
+    constexpr int NS = kMergeThreads / LPS;          // streams
+    static_assert(NS >= 1 && NS * LPS == kMergeThreads, "stream layout");
+    __shared__ float w[kMergeChunk];
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float4 part_num[NS > 1 ? NS - 1 : 1][LPS];
+    __shared__ float s_max, s_den;
+
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int cap = p.max_blocks * p.block_size;
+    int L = __ldg(p.seq_lens + s);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    const int n_parts = (L + p.partition_tokens - 1) / p.partition_tokens;
+    if (n_parts <= 1) return;  // the partition kernel wrote this row directly
+    const size_t row0 = (static_cast<size_t>(s) * p.hq + h) * p.max_partitions;
+    const float* ml = p.ws_ml + row0 * 2;
+
+    // reference max over the partitions
+    float M = -INFINITY;
+    for (int i = tid; i < n_parts; i += kMergeThreads) M = fmaxf(M, __ldcg(ml + 2 * i));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if ((tid & 31) == 0) red[tid >> 5] = M;
     __syncthreads();
     if (tid == 0) {
-        const unsigned prev = atomicAdd(p.counters + static_cast<size_t>(s) * p.hq + kvh * G, 1u);
-        s_last = prev == static_cast<unsigned>(n_parts - 1);
+        float m = red[0];
+#pragma unroll
+        for (int k = 1; k < kMergeThreads / 32; ++k) m = fmaxf(m, red[k]);
+        s_max = m;
     }
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    const int P = p.max_partitions;
-    const size_t row0 = (static_cast<size_t>(s) * p.hq + kvh * G) * P;  // row of (head 0, partition 0)
-    const float* ml = p.ws_ml;
-    const float* acc = p.ws_acc;
-    float* sM = sm;                          // [G] reference max per head
-    float* sDen = sm + G;                    // [G] normaliser per head
-    float* w = sm + 2 * G;                   // [G][kMergeChunk] partition weights
-    float* wl = w + G * kMergeChunk;         // [G][kMergeChunk] weighted normalisers
-    const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
-
-    for (int g = warp; g < G; g += nw) {
-        float M = -INFINITY;
-        for (int i = lane; i < n_parts; i += 32) M = fmaxf(M, __ldcg(ml + (row0 + g * P + i) * 2));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        if (lane == 0) {
-            sM[g] = M;
-            sDen[g] = 0.f;
-        }
+    M = s_max;
+    T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + h) * D;
+    if (M == -INFINITY) {
+        for (int d = tid; d < D; d += kMergeThreads) out[d] = Elt<T>::from_f32(0.f);
+        return;
     }
-    constexpr int kMaxOut = (G * D + 63) / 64;  // outputs per thread
-    float num[kMaxOut];
-#pragma unroll
-    for (int k = 0; k < kMaxOut; ++k) num[k] = 0.f;
+
+    const int stream = tid / LPS, lane4 = tid - stream * LPS;
+    const float4* acc = reinterpret_cast<const float4*>(p.ws_acc + row0 * D) + lane4;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den_part = 0.f;
     for (int c0 = 0; c0 < n_parts; c0 += kMergeChunk) {
         const int nc = min(kMergeChunk, n_parts - c0);
-        __syncthreads();  // sM ready; previous chunk consumed
-        for (int i = tid; i < G * nc; i += nthreads) {
-            const int g = i / nc, j = i - g * nc;
-            const size_t r = row0 + g * P + c0 + j;
-            const float M = sM[g];
-            const float f = (M == -INFINITY) ? 0.f : exp2f(__ldcg(ml + r * 2) - M);
-            w[g * kMergeChunk + j] = f;
-            wl[g * kMergeChunk + j] = f * __ldcg(ml + r * 2 + 1);
+        __syncthreads();  // previous chunk's weights consumed
+        for (int i = tid; i < nc; i += kMergeThreads) {
+            const float f = exp2f(__ldcg(ml + 2 * (c0 + i)) - M);
+            w[i] = f;
+            den_part = fmaf(f, __ldcg(ml + 2 * (c0 + i) + 1), den_part);
         }
         __syncthreads();
-        for (int g = warp; g < G; g += nw) {
-            float t = 0.f;
-            for (int j = lane; j < nc; j += 32) t += wl[g * kMergeChunk + j];
+        int i = stream;
+        for (; i + 7 * NS < nc; i += 8 * NS) {
+            float4 x[8];
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            if (lane == 0) sDen[g] += t;
-        }
+            for (int u = 0; u < 8; ++u) x[u] = __ldcg(acc + static_cast<size_t>(c0 + i + u * NS) * LPS);
 #pragma unroll
-        for (int k = 0; k < kMaxOut; ++k) {
-            const int idx = tid + k * nthreads;
-            if (idx < G * D) {
-                const int g = idx / D, d = idx - g * D;
-                const float* a = acc + (row0 + g * P + c0) * D + d;
-                const float* wg = w + g * kMergeChunk;
-                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                int j = 0;
-                for (; j + 4 <= nc; j += 4) {
-                    x0 = fmaf(wg[j], __ldcg(a + static_cast<size_t>(j) * D), x0);
-                    x1 = fmaf(wg[j + 1], __ldcg(a + static_cast<size_t>(j + 1) * D), x1);
-                    x2 = fmaf(wg[j + 2], __ldcg(a + static_cast<size_t>(j + 2) * D), x2);
-                    x3 = fmaf(wg[j + 3], __ldcg(a + static_cast<size_t>(j + 3) * D), x3);
-                }
-                for (; j < nc; ++j) x0 = fmaf(wg[j], __ldcg(a + static_cast<size_t>(j) * D), x0);
-                num[k] += (x0 + x1) + (x2 + x3);
+            for (int u = 0; u < 8; ++u) {
+                const float f = w[i + u * NS];
+                num.x = fmaf(f, x[u].x, num.x);
+                num.y = fmaf(f, x[u].y, num.y);
+                num.z = fmaf(f, x[u].z, num.z);
+                num.w = fmaf(f, x[u].w, num.w);
             }
         }
-    }
-    __syncthreads();
-    T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + kvh * G) * D;
-#pragma unroll
-    for (int k = 0; k < kMaxOut; ++k) {
-        const int idx = tid + k * nthreads;
-        if (idx < G * D) {
-            const float den = sDen[idx / D];
-            out[idx] = Elt<T>::from_f32(den > 0.f ? num[k] / den : 0.f);
+        for (; i < nc; i += NS) {
+            const float4 x = __ldcg(acc + static_cast<size_t>(c0 + i) * LPS);
+            const float f = w[i];
+            num.x = fmaf(f, x.x, num.x);
+            num.y = fmaf(f, x.y, num.y);
+            num.z = fmaf(f, x.z, num.z);
+            num.w = fmaf(f, x.w, num.w);
         }
     }
+    // normaliser: block sum of the per-thread partial sums
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den_part += __shfl_xor_sync(0xffffffffu, den_part, o);
+    __syncthreads();
+    if ((tid & 31) == 0) red[tid >> 5] = den_part;
+    if (stream > 0) part_num[stream - 1][lane4] = num;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMergeThreads / 32; ++k) t += red[k];
+        s_den = t;
+    }
+    __syncthreads();
+    if (stream == 0) {
+#pragma unroll
+        for (int k = 0; k < NS - 1; ++k) {
+            const float4 y = part_num[k][lane4];
+            num.x += y.x;
+            num.y += y.y;
+            num.z += y.z;
+            num.w += y.w;
+        }
+        const float den = s_den;
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        T* o = out + 4 * lane4;
+        o[0] = Elt<T>::from_f32(num.x * inv);
+        o[1] = Elt<T>::from_f32(num.y * inv);
+        o[2] = Elt<T>::from_f32(num.z * inv);
+        o[3] = Elt<T>::from_f32(num.w * inv);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+    decode_merge<T, D><<<dim3(p.hq, p.batch), kMergeThreads, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -122,7 +122,6 @@ struct MmaCfg {
     static constexpr int KSTEPS = D / 16;
     static constexpr int RED_BYTES = NW * G * (D + 2) * 4;
     static_assert(RED_BYTES <= RING_BYTES, "merge scratch aliases the ring");
-    static_assert((2 + 2 * kMergeChunk) * G * 4 <= RING_BYTES, "fused merge scratch aliases the ring");
     static_assert(G >= 1 && G <= 8, "query group on the N = 8 side");
     // + 1 KiB so the ring can be aligned to 1024 bytes for the 128-byte swizzle
     static constexpr size_t smem_bytes(int table_entries) {
@@ -387,7 +386,6 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
             }
         }
     }
-    if (!direct) merge_if_last<T, D, G>(p, s, kvh, n_parts, reinterpret_cast<float*>(smem), tid, blockDim.x);
 
 }
 
@@ -408,7 +406,9 @@ cudaError_t launch_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUt
     }
     dim3 grid(p.max_partitions, p.hkv, p.batch);
     decode_partition_mma<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p, kmap, vmap);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.max_partitions <= 1) return e;
+    return launch_merge<T, D>(p, stream);
 }
 
 }  // namespace pa

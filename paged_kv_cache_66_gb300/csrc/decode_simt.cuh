@@ -56,7 +56,6 @@ struct SimtCfg {
     static constexpr int RED_BYTES = NW * G * (D + 2) * 4;
     static_assert(NV >= 1 && DPL % VEC == 0, "lane layout");
     static_assert(RED_BYTES <= RING_BYTES, "merge scratch aliases the ring");
-    static_assert((2 + 2 * kMergeChunk) * G * 4 <= RING_BYTES, "fused merge scratch aliases the ring");
     static constexpr size_t smem_bytes(int table_entries) {
         return static_cast<size_t>(TBL_OFF) + static_cast<size_t>(table_entries) * 4;
     }
@@ -309,7 +308,6 @@ __global__ void __launch_bounds__(SimtCfg<T, D, G>::NW * 32)
             }
         }
     }
-    if (!direct) merge_if_last<T, D, G>(p, s, kvh, n_parts, reinterpret_cast<float*>(smem), tid, blockDim.x);
 
 }
 
@@ -330,7 +328,9 @@ cudaError_t launch_simt(const DecodeParams& p, cudaStream_t stream) {
     }
     dim3 grid(p.max_partitions, p.hkv, p.batch);
     decode_partition_simt<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.max_partitions <= 1) return e;
+    return launch_merge<T, D>(p, stream);
 }
 
 }  // namespace pa

@@ -61,12 +61,10 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Decode scratch: [counters B*Hq u32 | (max, normaliser) B*Hq*P*2 f32 | partials B*Hq*P*D f32],
-// each region 256-byte aligned.
+// Decode scratch: [(max, normaliser) B*Hq*P*2 f32 | partials B*Hq*P*D f32],
+// the second region 256-byte aligned.
 struct WsLayout {
     int partitions;
-    size_t cnt_bytes;
-    size_t ml_off;
     size_t acc_off;
     size_t total;
 };
@@ -76,9 +74,7 @@ WsLayout ws_layout(int batch, int hq, int d, int max_blocks, int b, int part) {
     w.partitions = static_cast<int>(ceil_div(static_cast<int64_t>(max_blocks) * b, part));
     if (w.partitions <= 1) return w;
     const size_t rows = static_cast<size_t>(batch) * hq * w.partitions;
-    w.cnt_bytes = static_cast<size_t>(batch) * hq * sizeof(unsigned);
-    w.ml_off = align256(w.cnt_bytes);
-    w.acc_off = w.ml_off + align256(rows * 2 * sizeof(float));
+    w.acc_off = align256(rows * 2 * sizeof(float));
     w.total = w.acc_off + rows * static_cast<size_t>(d) * sizeof(float);
     return w;
 }
@@ -200,8 +196,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     char* wsb = static_cast<char*>(workspace);
-    p.counters = ws.partitions > 1 ? reinterpret_cast<unsigned*>(wsb) : nullptr;
-    p.ws_ml = ws.partitions > 1 ? reinterpret_cast<float*>(wsb + ws.ml_off) : nullptr;
+    p.ws_ml = ws.partitions > 1 ? reinterpret_cast<float*>(wsb) : nullptr;
     p.ws_acc = ws.partitions > 1 ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
     p.err = err;
     p.num_blocks = num_blocks;
@@ -216,7 +211,6 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
     p.scale_log2 = scale * 1.4426950408889634f;
     p.kernel = g_decode_kernel.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (ws.partitions > 1 && cudaMemsetAsync(p.counters, 0, ws.cnt_bytes, st) != cudaSuccess) return PA_ERR_CUDA;
     switch (dtype) {
         case PA_F32: return from_cuda(pa::launch_decode_f32(p, st));
         case PA_F16: return from_cuda(pa::launch_decode_f16(p, st));

@@ -26,7 +26,6 @@ struct DecodeParams {
     const int32_t* seq_lens;      // [B]
     float* ws_ml;               // [B, Hq, P, 2] running max (log2 units) and normaliser
     float* ws_acc;              // [B, Hq, P, D] unnormalised partial outputs
-    unsigned int* counters;     // [B, Hq] partitions finished per (sequence, KV-head group), zeroed per call
     int* err;
     int64_t num_blocks;
     int max_blocks;

@@ -74,12 +74,11 @@ def test_workspace_size():
     lib = _lib.load()
     # one partition: no workspace
     assert lib.pa_decode_workspace_size(8, 32, 128, 32, 16, 512) == 0
-    # 8 x 32 heads: one counter each; x 64 partitions: (max, normaliser) + 128 partial floats
+    # 8 x 32 heads x 64 partitions: (max, normaliser) + 128 partial floats each
     rows = 8 * 32 * 64
-    cnt = (8 * 32 * 4 + 255) // 256 * 256
     ml = (rows * 8 + 255) // 256 * 256
-    assert lib.pa_decode_workspace_size(8, 32, 128, 2048, 16, 512) == cnt + ml + rows * 128 * 4
-    assert lib.pa_decode_workspace_size(8, 32, 128, 2048, 16, 0) == cnt + ml + rows * 128 * 4
+    assert lib.pa_decode_workspace_size(8, 32, 128, 2048, 16, 512) == ml + rows * 128 * 4
+    assert lib.pa_decode_workspace_size(8, 32, 128, 2048, 16, 0) == ml + rows * 128 * 4
 
 
 # ------------------------------------------------------------------ host manager
