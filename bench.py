@@ -285,6 +285,9 @@ def run_ours(args, ws, rank, local):
     t_start.record(stream)
     for j in range(args.steps):
         ds = dsteps[args.warmup + j]
+        for w in ds.plan.writes or []:          # arrivals' prompt writes (continuous batching)
+            rp._write_device(w)
+            launches += (1 if len(w.pairs) else 0) + nL * ((len(w.slots) + (1 << 14) - 1) >> 14)
         B, width = ds.tables.shape
         wsbuf = rp.workspace_for(B, width)
         if ds.pairs.shape[0]:
@@ -432,6 +435,95 @@ def run_e2e(args, wl, rp, dev, ws):
             "d2h_bytes_per_step": d2h // args.steps, "ms_per_step": ms / args.steps}
 
 
+def run_op(args, local):
+    """Single-kernel measurements of the rows other than decode (not the default
+    line): "append" = pa_kv_append of 8 x 4096 new tokens into a long-context
+    pool; "copy" = pa_copy_blocks of 64 copy-on-write pairs over 32 layers;
+    "host" = the C++ plan of one decode step (pa_host_decode_step) for the
+    long-context and prefix-shared batches."""
+    from paged_kv_cache_66_gb300 import api
+    from paged_kv_cache_66_gb300.host import HostBlockManager
+    peak, peak_kind = _peaks()
+    K = max(args.steps, 5)
+    if args.op != "host":
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+
+    line = {"op": args.op, "n_gpus": 1, "steps": K, "warmup": args.warmup, "data": "synthetic"}
+    if args.op == "append":
+        N, Hkv, b, D = 20000, 8, 16, 128
+        T = 8 * 4096
+        kp = torch.zeros((N, Hkv, b, D), dtype=torch.float16, device=dev)
+        vp = torch.zeros_like(kp)
+        k = torch.randn((T, Hkv, D), device=dev).half()
+        v = torch.randn((T, Hkv, D), device=dev).half()
+        slots = (torch.randperm(N, device=dev)[: T // b].repeat_interleave(b) * b +
+                 torch.arange(T, device=dev) % b).to(torch.int64)
+        ms = timed(lambda: api.pa_kv_append(k, v, kp, vp, slots))
+        alg = 2 * 2 * T * Hkv * D * 2 + 8 * T
+        line.update(metric="pa_kv_append GB/s", value=alg / (ms / 1e3) / 1e9, unit="GB/s", ms_per_launch=ms,
+                    config={"tokens": T, "kv_heads": Hkv, "head_dim": D, "block_size": b, "dtype": "f16"},
+                    roofline={"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                              "frac": alg / (ms / 1e3) / 1e9 / peak, "alg_bytes_per_launch": alg,
+                              "peak_kind": f"{peak_kind} hbm_gbs"})
+    elif args.op == "copy":
+        N, Hkv, b, D, L, n = 4096, 8, 16, 128, 32, 64
+        kps = [torch.randn((N, Hkv, b, D), device=dev).half() for _ in range(L)]
+        vps = [torch.randn((N, Hkv, b, D), device=dev).half() for _ in range(L)]
+        perm = torch.randperm(N, device=dev)
+        pairs = torch.stack([perm[:n], perm[n:2 * n]], 1).to(torch.int64).contiguous()
+        ms = timed(lambda: api.pa_copy_blocks(kps, vps, pairs))
+        alg = n * L * 2 * 2 * Hkv * b * D * 2
+        line.update(metric="pa_copy_blocks GB/s", value=alg / (ms / 1e3) / 1e9, unit="GB/s", ms_per_launch=ms,
+                    config={"pairs": n, "layers": L, "block_bytes": Hkv * b * D * 2, "dtype": "f16"},
+                    roofline={"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                              "frac": alg / (ms / 1e3) / 1e9 / peak, "alg_bytes_per_launch": alg,
+                              "peak_kind": f"{peak_kind} hbm_gbs"})
+    else:
+        res = {}
+        for name, wl in (("longctx-f16-b8x32k", wcfg.config3(steps=K + args.warmup, layers=1)),
+                         ("prefix-shared-bf16-b256", wcfg.config4(steps=K + args.warmup))):
+            h = HostBlockManager(wl.num_blocks, wl.b, wl.free_order)
+            for op in wl.setup_ops:           # host state only (no device writes)
+                if op[0] == "create":
+                    h.create(op[1])
+                elif op[0] == "write":
+                    h.reserve(op[1], op[2])
+                    h.advance(op[1], op[2])
+                elif op[0] == "fork":
+                    h.fork(op[1], op[2])
+                elif op[0] == "truncate":
+                    h.truncate(op[1], op[2])
+            uids = list(wl.step_ops[0][-1][1])
+            B = len(uids)
+            stride = max(len(h.table(u)) for u in uids) + K + args.warmup + 2
+            tables = np.zeros((B, stride), np.int32)
+            lens = np.zeros(B, np.int32)
+            slots = np.zeros(B, np.int64)
+            for _ in range(args.warmup):
+                h.decode_step(uids, tables, lens, slots)
+            t0 = time.perf_counter()
+            for _ in range(K):
+                h.decode_step(uids, tables, lens, slots)
+            res[name] = {"batch": B, "us_per_step": 1e6 * (time.perf_counter() - t0) / K}
+        line.update(metric="host decode-step plan us", value=res["longctx-f16-b8x32k"]["us_per_step"], unit="us",
+                    higher_is_better=False, config=res)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,12 +536,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
+    ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host"],
+                    help="step = the benchmark line; others measure one row of the path alone")
     args = ap.parse_args()
     D, G, b, dt = args.combo.split(",")
     args.combo = (int(D), int(G), int(b), dt)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
     ws, rank, local = _dist()
+    if args.op != "step":
+        run_op(args, local)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
     else:

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         const int64_t* __restrict__ slots, int64_t num_tokens,
                                                         int64_t num_slots, int hkv, int vpr, int block_size,
                                                         int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t total = num_tokens * hkv * 2 * vpr;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -51,6 +53,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
 __global__ void __launch_bounds__(256) copy_blocks_kernel(PoolPtrs pools, int num_layers,
                                                           const int64_t* __restrict__ pairs, int64_t num_blocks,
                                                           int64_t vec_per_block, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t y = blockIdx.y;
     const int64_t pair = y / (2 * num_layers);
     const int rem = static_cast<int>(y - pair * 2 * num_layers);
@@ -86,10 +90,10 @@ cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = 152LL * 16;
     if (blocks > cap) blocks = cap;
-    kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
-        static_cast<uint4*>(v_pool), slots, num_tokens, num_blocks * block_size, hkv, vpr, block_size, err);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
+                      static_cast<uint4*>(v_pool), slots, num_tokens, num_blocks * block_size, hkv, vpr,
+                      block_size, err);
 }
 
 cudaError_t launch_copy_blocks(const PoolPtrs& pools, int num_layers, const int64_t* pairs, int64_t num_pairs,
@@ -105,8 +109,8 @@ cudaError_t launch_copy_blocks(const PoolPtrs& pools, int num_layers, const int6
     for (int64_t p0 = 0; p0 < num_pairs; p0 += max_pairs) {
         const int64_t np = (num_pairs - p0 < max_pairs) ? (num_pairs - p0) : max_pairs;
         dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(np * per_pair));
-        copy_blocks_kernel<<<grid, threads, 0, stream>>>(pools, num_layers, pairs + 2 * p0, num_blocks, vec, err);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), 0, stream, pools, num_layers,
+                                   pairs + 2 * p0, num_blocks, vec, err);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

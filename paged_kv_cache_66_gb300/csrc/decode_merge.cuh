@@ -7,10 +7,13 @@
 // One CTA of 128 threads per (query head, sequence).  The partition weights
 // exp2(m_p - M) go to shared memory once; then the CTA's threads form
 // 128 / (D/4) "streams" of D/4 lanes, each lane owning 4 output dimensions,
-// and stream k walks partitions k, k + streams, ... with 8 float4 loads in
-// flight per lane.  Streams are combined in a fixed order, so the result is
-// deterministic.  (A variant fused into the partition kernel -- the last CTA
-// of a group merging -- measured slower: its merge sat on the kernel's tail.)
+// and stream k walks partitions k, k + streams, ...  When a lane has at most
+// 16 partials (up to 64 partitions at D = 128) all of them are requested
+// before the reference max is known, so the kernel pays about one memory
+// round trip; longer sequences loop with 8 float4 loads in flight per lane.
+// Streams are combined in a fixed order, so the result is deterministic.
+// (A variant fused into the partition kernel -- the last CTA of a group
+// merging -- measured slower: its merge sat on the kernel's tail.)
 #pragma once
 
 #include "pa_common.cuh"
@@ -20,17 +23,21 @@ namespace pa {
 
 constexpr int kMergeThreads = 128;
 constexpr int kMergeChunk = 1024;  // partitions whose weights sit in shared memory at once
+constexpr int kPrefetch = 16;      // partials per lane requested up front in the common case
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge(const DecodeParams p) {
     constexpr int LPS = D / 4;                       // lanes per stream (4 dims each)
     constexpr int NS = kMergeThreads / LPS;          // streams
     static_assert(NS >= 1 && NS * LPS == kMergeThreads, "stream layout");
+    static_assert(kPrefetch * NS <= kMergeThreads, "common case: one (max, normaliser) pair per thread");
     __shared__ float w[kMergeChunk];
     __shared__ float red[kMergeThreads / 32];
     __shared__ float4 part_num[NS > 1 ? NS - 1 : 1][LPS];
     __shared__ float s_max, s_den;
 
+    griddep_wait();
+    griddep_launch_dependents();
     const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
     const int cap = p.max_blocks * p.block_size;
     int L = __ldg(p.seq_lens + s);
@@ -39,6 +46,76 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge(const DecodeParams
     if (n_parts <= 1) return;  // the partition kernel wrote this row directly
     const size_t row0 = (static_cast<size_t>(s) * p.hq + h) * p.max_partitions;
     const float* ml = p.ws_ml + row0 * 2;
+    T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + h) * D;
+    const int stream = tid / LPS, lane4 = tid - stream * LPS;
+    const float4* acc = reinterpret_cast<const float4*>(p.ws_acc + row0 * D) + lane4;
+
+    if (n_parts <= kPrefetch * NS) {
+        // Common case: every partial of this lane is requested at once, before
+        // the reference max is known, together with the (max, normaliser) pairs.
+        float4 x[kPrefetch];
+#pragma unroll
+        for (int u = 0; u < kPrefetch; ++u) {
+            const int i = stream + u * NS;
+            x[u] = i < n_parts ? __ldcg(acc + static_cast<size_t>(i) * LPS) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mi = -INFINITY, li = 0.f;
+        if (tid < n_parts) {
+            mi = __ldcg(ml + 2 * tid);
+            li = __ldcg(ml + 2 * tid + 1);
+        }
+        float M = mi;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        if ((tid & 31) == 0) red[tid >> 5] = M;
+        __syncthreads();
+        M = red[0];
+#pragma unroll
+        for (int k = 1; k < kMergeThreads / 32; ++k) M = fmaxf(M, red[k]);
+        if (M == -INFINITY) {
+            for (int d = tid; d < D; d += kMergeThreads) out[d] = Elt<T>::from_f32(0.f);
+            return;
+        }
+        const float f = tid < n_parts ? exp2f(mi - M) : 0.f;
+        if (tid < kMergeChunk) w[tid] = f;
+        float dl = f * li;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+        __syncthreads();  // everyone has read red[] as maxima; w[] written
+        if ((tid & 31) == 0) red[tid >> 5] = dl;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kPrefetch; ++u) {
+            const int i = stream + u * NS;
+            const float g = i < n_parts ? w[i] : 0.f;
+            num.x = fmaf(g, x[u].x, num.x);
+            num.y = fmaf(g, x[u].y, num.y);
+            num.z = fmaf(g, x[u].z, num.z);
+            num.w = fmaf(g, x[u].w, num.w);
+        }
+        if (stream > 0) part_num[stream - 1][lane4] = num;
+        __syncthreads();
+        if (stream == 0) {
+#pragma unroll
+            for (int k = 0; k < NS - 1; ++k) {
+                const float4 y = part_num[k][lane4];
+                num.x += y.x;
+                num.y += y.y;
+                num.z += y.z;
+                num.w += y.w;
+            }
+            float den = 0.f;
+#pragma unroll
+            for (int k = 0; k < kMergeThreads / 32; ++k) den += red[k];
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            T* o = out + 4 * lane4;
+            o[0] = Elt<T>::from_f32(num.x * inv);
+            o[1] = Elt<T>::from_f32(num.y * inv);
+            o[2] = Elt<T>::from_f32(num.z * inv);
+            o[3] = Elt<T>::from_f32(num.w * inv);
+        }
+        return;
+    }
 
     // reference max over the partitions
     float M = -INFINITY;
@@ -55,14 +132,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge(const DecodeParams
     }
     __syncthreads();
     M = s_max;
-    T* out = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + h) * D;
     if (M == -INFINITY) {
         for (int d = tid; d < D; d += kMergeThreads) out[d] = Elt<T>::from_f32(0.f);
         return;
     }
 
-    const int stream = tid / LPS, lane4 = tid - stream * LPS;
-    const float4* acc = reinterpret_cast<const float4*>(p.ws_acc + row0 * D) + lane4;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den_part = 0.f;
     for (int c0 = 0; c0 < n_parts; c0 += kMergeChunk) {
@@ -132,8 +206,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge(const DecodeParams
 
 template <typename T, int D>
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
-    decode_merge<T, D><<<dim3(p.hq, p.batch), kMergeThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(decode_merge<T, D>, dim3(p.hq, p.batch), dim3(kMergeThreads), 0, stream, p);
 }
 
 }  // namespace pa

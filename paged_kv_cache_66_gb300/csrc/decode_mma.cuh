@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
     unsigned char* smem =
         smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-byte aligned ring
 
+    griddep_wait();
     const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size, P = p.partition_tokens;
@@ -323,6 +324,8 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
         }
     }
 
+    griddep_launch_dependents();
+
     // ---- normalisers: sum over the 8 token rows held by lanes with the same t
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -405,8 +408,7 @@ cudaError_t launch_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUt
         configured_for = dev;
     }
     dim3 grid(p.max_partitions, p.hkv, p.batch);
-    decode_partition_mma<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p, kmap, vmap);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_partition_mma<T, D, G>, grid, dim3(C::NW * 32), smem, stream, p, kmap, vmap);
     if (e != cudaSuccess || p.max_partitions <= 1) return e;
     return launch_merge<T, D>(p, stream);
 }

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(SimtCfg<T, D, G>::NW * 32)
     constexpr int NW = C::NW, STAGES = C::STAGES;
     extern __shared__ __align__(128) unsigned char smem[];
 
+    griddep_wait();
     const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size, P = p.partition_tokens;
@@ -249,6 +250,8 @@ __global__ void __launch_bounds__(SimtCfg<T, D, G>::NW * 32)
     }
     (void)timed_out;
 
+    griddep_launch_dependents();
+
     // ---- reduce over the token groups of the warp
 #pragma unroll
     for (int o = TG; o < 32; o <<= 1) {
@@ -327,8 +330,7 @@ cudaError_t launch_simt(const DecodeParams& p, cudaStream_t stream) {
         configured_for = dev;
     }
     dim3 grid(p.max_partitions, p.hkv, p.batch);
-    decode_partition_simt<T, D, G><<<grid, C::NW * 32, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_partition_simt<T, D, G>, grid, dim3(C::NW * 32), smem, stream, p);
     if (e != cudaSuccess || p.max_partitions <= 1) return e;
     return launch_merge<T, D>(p, stream);
 }

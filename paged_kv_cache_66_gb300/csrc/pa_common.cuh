@@ -139,6 +139,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Programmatic dependent launch: every kernel here is launched so that it may
+// be scheduled while the previous kernel of the stream drains; it waits for
+// that kernel (completion and memory) before touching any data, and signals
+// its own dependents once its remaining work no longer needs new CTAs.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Online softmax keeps a stale reference max until a tile's max exceeds it by
 // more than this many log2 units (exponents stay <= 2^8; exact after O / l).
 constexpr float kLazyRescale = 8.0f;

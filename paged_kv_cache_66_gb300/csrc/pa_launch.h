@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pagedkv.h"
 
 namespace pa {
@@ -36,6 +38,24 @@ struct DecodeParams {
     float scale_log2;           // scale * log2(e)
     int kernel;                 // pa_decode_kernel choice (PA_DECODE_AUTO / _SIMT / _MMA)
 };
+
+// Launch `kernel` on `stream` allowing programmatic dependent launch (the
+// kernel itself waits for its predecessor with griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // 2-D TMA descriptor of a pool viewed as [rows, D] 16-bit elements, boxes of
 // 16 rows x 64 elements (128 bytes) with the 128-byte swizzle.

@@ -2,6 +2,8 @@
 
 One decode step ("25. Paged attention and prefix caching", section "The paged
 cache", flow per step):
+  0. host + device: frees and arrivals of the step; an arrival's prompt write
+     (reserve + slots on the host, copy-on-write + pa_kv_append on the device)
   1. host: reserve one position per sequence (copy-on-write pairs), slot of
      the new position, length + 1, padded block tables   (C++ manager)
   2. device: pa_copy_blocks over every layer for the step's pairs
@@ -24,6 +26,19 @@ from .host import HostBlockManager
 
 
 @dataclass
+class PendingWrite:
+    """A prompt write planned on the host, executed on the device with its step."""
+    pairs: np.ndarray          # [n, 2] int64 copy-on-write pairs
+    slots: np.ndarray          # [T] int64
+    owners: np.ndarray         # [T] content owner of each position
+    positions: np.ndarray      # [T] int64
+    k_rows: list = None        # per layer [T, Hkv, D] on the device, once generated
+    v_rows: list = None
+    slots_d: torch.Tensor = None   # device copies, once uploaded
+    pairs_d: torch.Tensor = None
+
+
+@dataclass
 class StepPlan:
     step: int
     uids: list
@@ -32,6 +47,7 @@ class StepPlan:
     tables: np.ndarray         # [B, width] int32
     lens: np.ndarray           # [B] int32
     positions: np.ndarray      # [B] int64 (position of the appended token)
+    writes: list = None        # prompt writes of arrivals, run before the decode step
 
 
 @dataclass
@@ -66,23 +82,36 @@ class Replay:
             p = torch.as_tensor(np.asarray(pairs, dtype=np.int64).reshape(-1, 2)).to(self.device)
             api.pa_copy_blocks(self.k_pools, self.v_pools, p)
 
-    def _write(self, uid: int, n: int):
-        wl = self.wl
+    def _write_host(self, uid: int, n: int) -> "PendingWrite":
+        """Host part of a prompt write: reserve, slots, commit the length."""
         start = self.host.length(uid)
-        pairs = self.host.reserve(uid, n)
+        pairs = np.array(self.host.reserve(uid, n), dtype=np.int64).reshape(-1, 2)
         slots = self.host.slots(uid, start, n)
-        self._copy(np.array(pairs, dtype=np.int64))
         pos = np.arange(start, start + n, dtype=np.int64)
-        owners = wl.content_owners(uid, pos)
-        slots_d = torch.as_tensor(slots).to(self.device)
+        self.host.advance(uid, n)
+        return PendingWrite(pairs, slots, self.wl.content_owners(uid, pos), pos)
+
+    def _write_device(self, w: "PendingWrite", stream=None):
+        """Device part: copy-on-write copies, then the K/V rows of every layer."""
+        wl = self.wl
+        if len(w.pairs):
+            pairs_d = w.pairs_d if w.pairs_d is not None else torch.as_tensor(w.pairs).to(self.device)
+            api.pa_copy_blocks(self.k_pools, self.v_pools, pairs_d, stream=stream)
+        slots_d = w.slots_d if w.slots_d is not None else torch.as_tensor(w.slots).to(self.device)
+        n = len(w.slots)
         chunk = 1 << 14
         for li, layer in enumerate(self.layers):
             for c0 in range(0, n, chunk):
                 c1 = min(n, c0 + chunk)
-                k = wcfg.kv_rows(wl, layer, "k", owners[c0:c1], pos[c0:c1], device=self.device)
-                v = wcfg.kv_rows(wl, layer, "v", owners[c0:c1], pos[c0:c1], device=self.device)
-                api.pa_kv_append(k, v, self.k_pools[li], self.v_pools[li], slots_d[c0:c1])
-        self.host.advance(uid, n)
+                if w.k_rows is not None:
+                    k, v = w.k_rows[li][c0:c1], w.v_rows[li][c0:c1]
+                else:
+                    k = wcfg.kv_rows(wl, layer, "k", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
+                    v = wcfg.kv_rows(wl, layer, "v", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
+                api.pa_kv_append(k, v, self.k_pools[li], self.v_pools[li], slots_d[c0:c1], stream=stream)
+
+    def _write(self, uid: int, n: int):
+        self._write_device(self._write_host(uid, n))
 
     def apply(self, op):
         kind = op[0]
@@ -106,11 +135,15 @@ class Replay:
 
     # ------------------------------------------------------------------ steps
     def plan_step(self, step_index: int) -> StepPlan:
-        """Apply the step's non-decode ops (frees, arrivals with their prompt
-        writes), then the host part of the decode step."""
+        """Host part of one step: the step's frees and arrivals (their prompt
+        writes are planned, not yet executed), then the decode step itself."""
         ops = self.wl.step_ops[step_index]
         plan = None
+        writes = []
         for op in ops:
+            if op[0] == "write":
+                writes.append(self._write_host(op[1], int(op[2])))
+                continue
             if op[0] != "step":
                 self.apply(op)
                 continue
@@ -123,13 +156,18 @@ class Replay:
             slots = np.zeros(B, dtype=np.int64)
             pairs, w = self.host.decode_step(uids, tables, lens, slots)
             plan = StepPlan(self.steps_done, uids, slots, pairs, np.ascontiguousarray(tables[:, :w]), lens,
-                            positions)
+                            positions, writes)
             self.steps_done += 1
         return plan
 
     def device_step(self, plan: StepPlan) -> DeviceStep:
         """Upload the plan and generate the step's q and new K/V rows on the device."""
         wl, dev = self.wl, self.device
+        for w in plan.writes or []:
+            w.slots_d = torch.as_tensor(w.slots).to(dev)
+            w.pairs_d = torch.as_tensor(w.pairs).to(dev)
+            w.k_rows = [wcfg.kv_rows(wl, layer, "k", w.owners, w.positions, device=dev) for layer in self.layers]
+            w.v_rows = [wcfg.kv_rows(wl, layer, "v", w.owners, w.positions, device=dev) for layer in self.layers]
         owners = np.array([wl.content_owner(u, int(p)) for u, p in zip(plan.uids, plan.positions)])
         rows = np.arange(len(plan.uids))
         q, kn, vn = [], [], []
@@ -151,6 +189,8 @@ class Replay:
     def run_step(self, ds: DeviceStep, outs=None, stream=None) -> list:
         """Device part of one decode step over every layer; returns outputs."""
         wl = self.wl
+        for w in ds.plan.writes or []:
+            self._write_device(w, stream=stream)
         B, width = ds.tables.shape
         ws = self.workspace_for(B, width)
         if ds.pairs.shape[0]:
