@@ -195,6 +195,16 @@ typedef enum pa_decode_kernel {
 pa_status pa_set_decode_kernel(pa_decode_kernel kernel);
 
 /*
+ * pa_selftest_wait_timeout -- exercise the failure path of the bounded
+ * device waits: launch one warp that waits on an mbarrier nothing completes,
+ * giving up after `limit_us` microseconds (1..100000).  Afterwards
+ * pa_get_device_error reports PA_DEVERR_TIMEOUT (status PA_ERR_TIMEOUT) and
+ * the context stays usable.  The decode kernels use the same wait with a
+ * 1-second limit.
+ */
+pa_status pa_selftest_wait_timeout(int limit_us, void* stream);
+
+/*
  * pa_get_device_error -- synchronise `stream`, then read and clear the device
  * error word of the current device.  *code receives the OR of PA_DEVERR_* bits
  * raised since the last call (0 when none).  Returns PA_ERR_DEVICE_CHECK when

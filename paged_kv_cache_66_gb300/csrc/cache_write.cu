@@ -81,6 +81,25 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(PoolPtrs pools, int nu
     for (; i < vec_per_block; i += stride) d[i] = s[i];
 }
 
+// Failure-path check of the bounded waits: one warp initialises an mbarrier
+// that nothing will ever complete and waits on it with the same helper the
+// decode kernels use, for at most `limit_ns`.  The wait gives up, the kernel
+// records PA_DEVERR_TIMEOUT and returns; nothing hangs and nothing faults.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, int* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns) && threadIdx.x == 0) flag_error(err, PA_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slots,
                              int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,
                              int* err, cudaStream_t stream) {

@@ -219,6 +219,14 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
     }
 }
 
+pa_status pa_selftest_wait_timeout(int limit_us, void* stream) {
+    if (limit_us <= 0 || limit_us > 100000) return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    return from_cuda(pa::launch_wait_timeout_selftest(static_cast<uint64_t>(limit_us) * 1000ull, err,
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_get_device_error(int* code, void* stream) {
     if (!code) return PA_ERR_INVALID;
     *code = 0;

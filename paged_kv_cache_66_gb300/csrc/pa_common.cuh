@@ -106,14 +106,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` with a time limit (~1 s).  Returns false on
-// timeout; the caller records PA_DEVERR_TIMEOUT and winds down.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` with a time limit (default 1 s).  Returns
+// false on timeout; the caller records PA_DEVERR_TIMEOUT and winds down.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 1000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > 1000000000ull) return false;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

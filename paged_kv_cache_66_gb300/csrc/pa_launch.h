@@ -65,6 +65,8 @@ cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v
                              int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,
                              int* err, cudaStream_t stream);
 
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(const PoolPtrs& pools, int num_layers, const int64_t* pairs, int64_t num_pairs,
                                int64_t num_blocks, size_t block_bytes, int* err, cudaStream_t stream);
 

@@ -277,3 +277,23 @@ def test_decode_bad_table_entry_is_flagged_not_faulted(api, kernel):
     lens[0] = 10_000                                 # above the table's capacity
     _run_decode(api, q, K, V, tables, lens, 0.125)
     assert api.pa_get_device_error() & 4             # PA_DEVERR_SEQLEN
+
+
+def test_bounded_wait_gives_up_and_reports(api):
+    """A wait that nothing satisfies ends after its limit with a timeout status;
+    the context stays usable (a decode right after still matches the oracle)."""
+    from paged_kv_cache_66_gb300 import _lib
+    lib = _lib.load()
+    import ctypes as C
+    assert api.pa_get_device_error() == 0
+    st = lib.pa_selftest_wait_timeout(2000, C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    code = api.pa_get_device_error()
+    assert code == 16                                   # PA_DEVERR_TIMEOUT only
+    gen = torch.Generator().manual_seed(12)
+    t, K, V, tables, lens = _setup_paged([600, 3], 2, 64, 16, torch.float16, gen)
+    q = _rand((2, 4, 64), torch.float16, gen)
+    got = _run_decode(api, q, K, V, tables, lens, 0.125)
+    want = _oracle_decode(q, K, V, tables, lens, 16, 0.125)
+    assert np.abs(got.double().numpy() - want).max() <= 2e-3
+    assert api.pa_get_device_error() == 0
