@@ -285,9 +285,6 @@ def run_ours(args, ws, rank, local):
     t_start.record(stream)
     for j in range(args.steps):
         ds = dsteps[args.warmup + j]
-        for w in ds.plan.writes or []:          # arrivals' prompt writes (continuous batching)
-            rp._write_device(w)
-            launches += (1 if len(w.pairs) else 0) + nL * ((len(w.slots) + (1 << 14) - 1) >> 14)
         B, width = ds.tables.shape
         wsbuf = rp.workspace_for(B, width)
         if ds.pairs.shape[0]:

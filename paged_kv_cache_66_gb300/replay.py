@@ -2,12 +2,13 @@
 
 One decode step ("25. Paged attention and prefix caching", section "The paged
 cache", flow per step):
-  0. host + device: frees and arrivals of the step; an arrival's prompt write
-     (reserve + slots on the host, copy-on-write + pa_kv_append on the device)
+  0. host: frees and arrivals of the step; an arrival's prompt write is
+     reserved and given its slots
   1. host: reserve one position per sequence (copy-on-write pairs), slot of
      the new position, length + 1, padded block tables   (C++ manager)
-  2. device: pa_copy_blocks over every layer for the step's pairs
-  3. device, per layer: pa_kv_append of the new K/V rows, then pa_decode
+  2. device: one pa_copy_blocks over every layer for all the step's pairs
+  3. device, per layer: one pa_kv_append of all the step's new K/V rows
+     (arrivals' prompts and one token per sequence), then pa_decode
 The host part of a step is planned separately (``plan_step``) from its device
 part (``run_step``) so that a benchmark can keep the plans of many steps
 resident on the device and time the device path alone.
@@ -32,10 +33,6 @@ class PendingWrite:
     slots: np.ndarray          # [T] int64
     owners: np.ndarray         # [T] content owner of each position
     positions: np.ndarray      # [T] int64
-    k_rows: list = None        # per layer [T, Hkv, D] on the device, once generated
-    v_rows: list = None
-    slots_d: torch.Tensor = None   # device copies, once uploaded
-    pairs_d: torch.Tensor = None
 
 
 @dataclass
@@ -52,14 +49,15 @@ class StepPlan:
 
 @dataclass
 class DeviceStep:
-    """A step's metadata and inputs, resident on the device."""
+    """A step's metadata and inputs, resident on the device (appends and copies of
+    the whole step, arrivals' prompts included)."""
     plan: StepPlan
     slots: torch.Tensor
     pairs: torch.Tensor
     tables: torch.Tensor
     lens: torch.Tensor
     q: list                    # per layer [B, Hq, D]
-    k_new: list                # per layer [B, Hkv, D]
+    k_new: list                # per layer [T, Hkv, D]: arrivals' prompt rows, then one row per sequence
     v_new: list
 
 
@@ -95,19 +93,15 @@ class Replay:
         """Device part: copy-on-write copies, then the K/V rows of every layer."""
         wl = self.wl
         if len(w.pairs):
-            pairs_d = w.pairs_d if w.pairs_d is not None else torch.as_tensor(w.pairs).to(self.device)
-            api.pa_copy_blocks(self.k_pools, self.v_pools, pairs_d, stream=stream)
-        slots_d = w.slots_d if w.slots_d is not None else torch.as_tensor(w.slots).to(self.device)
+            api.pa_copy_blocks(self.k_pools, self.v_pools, torch.as_tensor(w.pairs).to(self.device), stream=stream)
+        slots_d = torch.as_tensor(w.slots).to(self.device)
         n = len(w.slots)
         chunk = 1 << 14
         for li, layer in enumerate(self.layers):
             for c0 in range(0, n, chunk):
                 c1 = min(n, c0 + chunk)
-                if w.k_rows is not None:
-                    k, v = w.k_rows[li][c0:c1], w.v_rows[li][c0:c1]
-                else:
-                    k = wcfg.kv_rows(wl, layer, "k", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
-                    v = wcfg.kv_rows(wl, layer, "v", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
+                k = wcfg.kv_rows(wl, layer, "k", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
+                v = wcfg.kv_rows(wl, layer, "v", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
                 api.pa_kv_append(k, v, self.k_pools[li], self.v_pools[li], slots_d[c0:c1], stream=stream)
 
     def _write(self, uid: int, n: int):
@@ -161,22 +155,26 @@ class Replay:
         return plan
 
     def device_step(self, plan: StepPlan) -> DeviceStep:
-        """Upload the plan and generate the step's q and new K/V rows on the device."""
+        """Upload the plan and generate the step's q and new K/V rows on the device.
+
+        Every row the step appends -- the prompts of arriving sequences and one
+        token per decoding sequence -- goes into one pa_kv_append per layer, and
+        every copy-on-write pair into one pa_copy_blocks (copies first: a
+        copy's source is a shared block, which no append of the step touches)."""
         wl, dev = self.wl, self.device
-        for w in plan.writes or []:
-            w.slots_d = torch.as_tensor(w.slots).to(dev)
-            w.pairs_d = torch.as_tensor(w.pairs).to(dev)
-            w.k_rows = [wcfg.kv_rows(wl, layer, "k", w.owners, w.positions, device=dev) for layer in self.layers]
-            w.v_rows = [wcfg.kv_rows(wl, layer, "v", w.owners, w.positions, device=dev) for layer in self.layers]
+        writes = plan.writes or []
         owners = np.array([wl.content_owner(u, int(p)) for u, p in zip(plan.uids, plan.positions)])
+        all_owners = np.concatenate([w.owners for w in writes] + [owners])
+        all_pos = np.concatenate([w.positions for w in writes] + [plan.positions])
+        all_slots = np.concatenate([w.slots for w in writes] + [plan.slots])
+        all_pairs = np.concatenate([w.pairs.reshape(-1, 2) for w in writes] + [plan.pairs.reshape(-1, 2)])
         rows = np.arange(len(plan.uids))
         q, kn, vn = [], [], []
         for layer in self.layers:
             q.append(wcfg.q_rows(wl, layer, plan.step, rows, device=dev))
-            kn.append(wcfg.kv_rows(wl, layer, "k", owners, plan.positions, device=dev))
-            vn.append(wcfg.kv_rows(wl, layer, "v", owners, plan.positions, device=dev))
-        return DeviceStep(plan, torch.as_tensor(plan.slots).to(dev),
-                          torch.as_tensor(plan.pairs.reshape(-1, 2)).to(dev),
+            kn.append(wcfg.kv_rows(wl, layer, "k", all_owners, all_pos, device=dev))
+            vn.append(wcfg.kv_rows(wl, layer, "v", all_owners, all_pos, device=dev))
+        return DeviceStep(plan, torch.as_tensor(all_slots).to(dev), torch.as_tensor(all_pairs).to(dev),
                           torch.as_tensor(plan.tables).to(dev), torch.as_tensor(plan.lens).to(dev), q, kn, vn)
 
     def workspace_for(self, batch: int, max_blocks: int) -> torch.Tensor:
@@ -189,8 +187,6 @@ class Replay:
     def run_step(self, ds: DeviceStep, outs=None, stream=None) -> list:
         """Device part of one decode step over every layer; returns outputs."""
         wl = self.wl
-        for w in ds.plan.writes or []:
-            self._write_device(w, stream=stream)
         B, width = ds.tables.shape
         ws = self.workspace_for(B, width)
         if ds.pairs.shape[0]:
