@@ -204,8 +204,80 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge(const DecodeParams
     }
 }
 
+// Batches whose sequences have at most kSmallParts partitions: one CTA of 128
+// threads merges 128 / (D/4) query heads of one sequence, each lane holding
+// 4 output dimensions and requesting all of its partials at once; the
+// (max, normaliser) pairs go through shared memory, so the kernel costs one
+// memory round trip and one barrier.  (With one CTA per head, config-5-like
+// batches launched 4096 tiny CTAs and the merge took ~12 us.)
+constexpr int kSmallParts = 16;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_small(const DecodeParams p) {
+    constexpr int LPS = D / 4;                 // lanes per head
+    constexpr int HPC = kMergeThreads / LPS;   // heads per CTA
+    __shared__ float sml[HPC][kSmallParts][2];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int s = blockIdx.y, h0 = blockIdx.x * HPC, tid = threadIdx.x;
+    const int cap = p.max_blocks * p.block_size;
+    int L = __ldg(p.seq_lens + s);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    const int n_parts = (L + p.partition_tokens - 1) / p.partition_tokens;
+    if (n_parts <= 1) return;  // the partition kernel wrote these rows directly (uniform per CTA)
+    const int hh = tid / LPS, lane4 = tid - hh * LPS, h = h0 + hh;
+    const bool active = h < p.hq;
+    const int P = p.max_partitions;
+    float4 x[kSmallParts];
+    if (active) {
+        const float4* acc =
+            reinterpret_cast<const float4*>(p.ws_acc + (static_cast<size_t>(s) * p.hq + h) * P * D) + lane4;
+#pragma unroll
+        for (int u = 0; u < kSmallParts; ++u)
+            x[u] = u < n_parts ? __ldcg(acc + static_cast<size_t>(u) * LPS) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int i = tid; i < HPC * n_parts; i += kMergeThreads) {
+        const int k = i / n_parts, u = i - k * n_parts;
+        if (h0 + k < p.hq) {
+            const float* ml = p.ws_ml + ((static_cast<size_t>(s) * p.hq + h0 + k) * P + u) * 2;
+            sml[k][u][0] = __ldcg(ml);
+            sml[k][u][1] = __ldcg(ml + 1);
+        }
+    }
+    __syncthreads();
+    if (!active) return;
+    float M = -INFINITY;
+    for (int u = 0; u < n_parts; ++u) M = fmaxf(M, sml[hh][u][0]);
+    T* o = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + h) * D + 4 * lane4;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int u = 0; u < kSmallParts; ++u) {
+            if (u < n_parts) {
+                const float f = exp2f(sml[hh][u][0] - M);
+                den = fmaf(f, sml[hh][u][1], den);
+                num.x = fmaf(f, x[u].x, num.x);
+                num.y = fmaf(f, x[u].y, num.y);
+                num.z = fmaf(f, x[u].z, num.z);
+                num.w = fmaf(f, x[u].w, num.w);
+            }
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    o[0] = Elt<T>::from_f32(num.x * inv);
+    o[1] = Elt<T>::from_f32(num.y * inv);
+    o[2] = Elt<T>::from_f32(num.z * inv);
+    o[3] = Elt<T>::from_f32(num.w * inv);
+}
+
 template <typename T, int D>
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+    if (p.max_partitions <= kSmallParts) {
+        constexpr int HPC = kMergeThreads / (D / 4);
+        return launch_pdl(decode_merge_small<T, D>, dim3((p.hq + HPC - 1) / HPC, p.batch), dim3(kMergeThreads), 0,
+                          stream, p);
+    }
     return launch_pdl(decode_merge<T, D>, dim3(p.hq, p.batch), dim3(kMergeThreads), 0, stream, p);
 }
 
