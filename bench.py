@@ -162,16 +162,17 @@ def _workload(cfg: int, steps: int, combo=None):
     return wcfg.config1()
 
 
-def _kv_bytes(wl, lens) -> int:
-    return int(np.sum(np.asarray(lens, dtype=np.int64))) * 2 * wl.Hkv * wl.D * wl.elt
+def _kv_bytes(wl, lens, elt=None) -> int:
+    """Effective K/V bytes one decode reads: sum of L * 2 * Hkv * D * (stored element size)."""
+    return int(np.sum(np.asarray(lens, dtype=np.int64))) * 2 * wl.Hkv * wl.D * (wl.elt if elt is None else elt)
 
 
-def _alg_bytes_decode(wl, plan) -> int:
+def _alg_bytes_decode(wl, plan, kv_elt=None) -> int:
     """Algorithmic bytes of one pa_decode launch: K/V history + q + out + block
     tables + lengths (scratch traffic of the split is not algorithmic)."""
     B = len(plan.uids)
     tbl = int(np.sum((np.asarray(plan.lens, dtype=np.int64) + wl.b - 1) // wl.b)) * 4
-    return _kv_bytes(wl, plan.lens) + 2 * B * wl.Hq * wl.D * wl.elt + tbl + 4 * B
+    return _kv_bytes(wl, plan.lens, kv_elt) + 2 * B * wl.Hq * wl.D * wl.elt + tbl + 4 * B
 
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
@@ -260,7 +261,7 @@ def run_ours(args, ws, rank, local):
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
         wl.layers = min(wl.layers, args.layers)
-    rp = Replay(wl, device=dev)
+    rp = Replay(wl, device=dev, kv=args.kv)
     rp.run_setup()
     torch.cuda.synchronize()
 
@@ -291,11 +292,10 @@ def run_ours(args, ws, rank, local):
             api.pa_copy_blocks(rp.k_pools, rp.v_pools, ds.pairs)
             launches += 1
         for li in range(nL):
-            api.pa_kv_append(ds.k_new[li], ds.v_new[li], rp.k_pools[li], rp.v_pools[li], ds.slots)
+            rp.append(li, ds.k_new[li], ds.v_new[li], ds.slots)
             a, b = ev_dec[j * nL + li]
             a.record(stream)
-            api.pa_decode(outs[li], ds.q[li], rp.k_pools[li], rp.v_pools[li], ds.tables, ds.lens, wl.scale,
-                          partition_tokens=rp.partition_tokens, workspace=wsbuf if wsbuf.numel() else None)
+            rp.decode(li, outs[li], ds.q[li], ds.tables, ds.lens, wsbuf)
             b.record(stream)
             launches += 2 + (1 if wsbuf.numel() else 0)
     t_end.record(stream)
@@ -304,14 +304,14 @@ def run_ours(args, ws, rank, local):
     clk = clocks.stop()
     dev_ms = t_start.elapsed_time(t_end)
     dev_ms_max = _max_over_ranks(dev_ms, ws, dev)
-    kv = sum(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens) for j in range(args.steps)) * nL
+    kv = sum(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens, rp.kv_elt) for j in range(args.steps)) * nL
     kv_all = _sum_over_ranks(float(kv), ws, dev)
     value = kv_all / (dev_ms_max / 1e3) / 1e9
     B = len(plans[0].uids)
     seq_steps = B * args.steps * ws / (dev_ms_max / 1e3)
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
     dec_avg = sum(dec_ms) / len(dec_ms)
-    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan) for j in range(args.steps))
+    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan, rp.kv_elt) for j in range(args.steps))
     peak, peak_kind = _peaks()
     achieved = alg / (dec_avg / 1e3) / 1e9
     err = api.pa_get_device_error()
@@ -324,10 +324,12 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dev_ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype if args.kv == "native" else f"{wl.dtype}+e4m3-kv",
+        "data": "synthetic",
         "config": {"workload": wl.name, "batch": B, "context": int(np.max(plans[0].lens)), "layers": nL,
                    "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
-                   "partition_tokens": rp.partition_tokens, "l2": "inputs larger than L2 (no flush needed)",
+                   "partition_tokens": rp.partition_tokens, "kv_cache": "e4m3" if args.kv == "fp8" else wl.dtype,
+                   "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{ws}"},
         "seq_steps_per_s": seq_steps,
         "pct_hbm_peak": 100.0 * value / peak,
@@ -405,7 +407,7 @@ def run_e2e(args, wl, rp, dev, ws):
         slots, lens, tables = meta_views(buf["meta"])
         ln = lens.numpy()
         pairs, width = rp.host.decode_step(uids, tables.numpy(), ln, slots.numpy())
-        kv += _kv_bytes(wl, ln) * nL
+        kv += _kv_bytes(wl, ln, rp.kv_elt) * nL
         d_meta.copy_(buf["meta"], non_blocking=True)
         buf["ev"] = torch.cuda.Event()
         buf["ev"].record(stream)
@@ -418,9 +420,8 @@ def run_e2e(args, wl, rp, dev, ws):
         h2d += host_in[j].numel() * wl.elt
         wsbuf = rp.workspace_for(B, stride)
         for li in range(nL):
-            api.pa_kv_append(d_k[li], d_v[li], rp.k_pools[li], rp.v_pools[li], d_slots)
-            api.pa_decode(d_out[li], d_q[li], rp.k_pools[li], rp.v_pools[li], d_tables, d_lens, wl.scale,
-                          partition_tokens=rp.partition_tokens, workspace=wsbuf if wsbuf.numel() else None)
+            rp.append(li, d_k[li], d_v[li], d_slots)
+            rp.decode(li, d_out[li], d_q[li], d_tables, d_lens, wsbuf)
         out_host.copy_(d_out, non_blocking=True)
         d2h += d_out.numel() * wl.elt
     t1.record(stream)
@@ -533,6 +534,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
+    ap.add_argument("--kv", default="native", choices=["native", "fp8"], help="KV cache storage (fp8 = E4M3)")
     ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host"],
                     help="step = the benchmark line; others measure one row of the path alone")
     args = ap.parse_args()

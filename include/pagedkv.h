@@ -177,6 +177,38 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const 
                             int partition_tokens, pa_dtype dtype, void* stream);
 
 /*
+ * FP8 (E4M3) KV cache -- the pools hold one byte per element, halving the
+ * bytes every decode reads ("25. Paged attention and prefix caching",
+ * "Attention that reads through the table": FP8 KV caches; "Модуль 09",
+ * "6. Квантование KV-кэша по блокам": E4M3 halves KV memory, the scale kept
+ * per head).  Layout of the pools as above, [num_blocks, Hkv, b, D] bytes;
+ * k_scale, v_scale are DEVICE fp32 arrays [Hkv] (one scale per KV head of
+ * the layer).  A stored code c of head h stands for e4m3(c) * scale[h].
+ *
+ * pa_kv_append_fp8 -- like pa_kv_append, quantising on the way: rows k, v
+ *   [T, Hkv, D] in `in_dtype` (f32, f16 or bf16) are stored as
+ *   e4m3(x / scale[h]), the quotient an IEEE fp32 division, rounded to the
+ *   nearest code (ties to even) and saturated to +-448.  D a multiple of 16.
+ *
+ * pa_decode_fp8 -- like pa_decode over FP8 pools: q and out [B, Hq, D] in
+ *   `q_dtype` (f16 or bf16); the attention is taken over the dequantised
+ *   history, with q used in f16 (exact for bf16 values in f16's normal range)
+ *   and fp32 accumulation.  Tensor-core kernel only: D in {128, 256}, Hq/Hkv in
+ *   {1, 2, 4, 8}, b a multiple of 16, num_blocks * Hkv * b < 2^31 (else
+ *   PA_ERR_UNSUPPORTED).  Workspace as for pa_decode.
+ */
+pa_status pa_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,
+                           const float* k_scale, const float* v_scale, const int64_t* slot_mapping,
+                           int64_t num_tokens, int64_t num_blocks, int num_kv_heads, int head_dim,
+                           int block_size, void* stream);
+
+pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* k_pool, const void* v_pool,
+                        const float* k_scale, const float* v_scale, int64_t num_blocks,
+                        const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                        int partition_tokens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_set_decode_kernel -- process-wide choice of the pa_decode partition
  * kernel (both compute the same result within the attention tolerance):
  *   PA_DECODE_AUTO  (default) tensor cores for fp16/bf16 pools, CUDA cores for fp32;

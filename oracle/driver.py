@@ -20,12 +20,17 @@ import numpy as np
 
 from workload import configs as wcfg
 
-from . import attention, cache_ops
+from . import attention, cache_ops, quant
 from .blocks import SeqTables
 
 
 class OracleRun:
-    def __init__(self, wl, pools: bool = True, layers=None):
+    def __init__(self, wl, pools: bool = True, layers=None, kv: str = "native"):
+        """kv = "fp8": the K/V history is what E4M3 pools with the workload's
+        per-(layer, KV head) scales store (content route only)."""
+        self.kv = kv
+        if kv == "fp8" and pools:
+            raise ValueError("the FP8 replay uses the content route (pools=False)")
         self.wl = wl
         self.t = SeqTables(wl.num_blocks, wl.b, wl.free_order)
         self.layers = list(range(wl.layers)) if layers is None else list(layers)
@@ -119,6 +124,11 @@ class OracleRun:
         wl = self.wl
         pos = np.arange(length, dtype=np.int64)
         owners = wl.content_owners(uid, pos)
-        K = wcfg.kv_rows(wl, layer, "k", owners, pos).double().numpy()
-        V = wcfg.kv_rows(wl, layer, "v", owners, pos).double().numpy()
-        return K, V
+        K = wcfg.kv_rows(wl, layer, "k", owners, pos)
+        V = wcfg.kv_rows(wl, layer, "v", owners, pos)
+        if self.kv == "fp8":
+            ks, vs = wcfg.kv_scales(wl, layer, "k"), wcfg.kv_scales(wl, layer, "v")
+            K = quant.dequantize(quant.quantize_rows(K.float().numpy(), ks), ks, head_axis=1)
+            V = quant.dequantize(quant.quantize_rows(V.float().numpy(), vs), vs, head_axis=1)
+            return K, V
+        return K.double().numpy(), V.double().numpy()

@@ -30,6 +30,9 @@ SIGNATURES = {
                          _vp, _sz, _i32, _vp]),
     "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                  _i32, _i32, _vp]),
+    "pa_kv_append_fp8": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
+    "pa_decode_fp8": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                             _f32, _i32, _vp, _sz, _vp]),
     "pa_set_decode_kernel": (_i32, [_i32]),
     "pa_selftest_wait_timeout": (_i32, [_i32, _vp]),
     "pa_get_device_error": (_i32, [C.POINTER(C.c_int), _vp]),

@@ -18,7 +18,7 @@ _TORCH_TO_ID = {torch.float32: DTYPE_IDS["f32"], torch.float16: DTYPE_IDS["f16"]
                 torch.bfloat16: DTYPE_IDS["bf16"]}
 
 __all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
-           "pa_set_decode_kernel", "pa_get_device_error", "pa_status_string", "PagedKVError"]
+           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_get_device_error", "pa_status_string", "PagedKVError"]
 
 
 def _stream(stream):
@@ -126,6 +126,49 @@ def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, par
                                 block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, Hkv, D, b,
                                 float(scale), int(partition_tokens), _dtype_id(k_pool), _stream(stream)),
           "pa_decode_noalloc")
+
+
+def pa_kv_append_fp8(k, v, k_pool, v_pool, k_scale, v_scale, slot_mapping, stream=None) -> None:
+    """Quantise k, v [T, Hkv, D] (f32/f16/bf16) to E4M3 bytes of pools
+    [N, Hkv, b, D] (uint8) with per-head scales k_scale, v_scale [Hkv] (f32)."""
+    lib = load()
+    N, Hkv, b, D = k_pool.shape
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8 or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("FP8 pools are uint8 tensors [N, Hkv, b, D]")
+    if k.shape != v.shape or k.dim() != 3 or k.shape[1:] != (Hkv, D) or slot_mapping.shape != (k.shape[0],):
+        raise ValueError("shape mismatch: k, v [T, Hkv, D]; slots [T]")
+    if k_scale.shape != (Hkv,) or v_scale.shape != (Hkv,):
+        raise ValueError("scales are [Hkv]")
+    check(lib.pa_kv_append_fp8(_dev(k, "k", k.dtype), _dev(v, "v", k.dtype), _dtype_id(k), _dev(k_pool, "k_pool"),
+                               _dev(v_pool, "v_pool"), _dev(k_scale, "k_scale", torch.float32),
+                               _dev(v_scale, "v_scale", torch.float32),
+                               _dev(slot_mapping, "slot_mapping", torch.int64), k.shape[0], N, Hkv, D, b,
+                               _stream(stream)), "pa_kv_append_fp8")
+
+
+def pa_decode_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, scale, partition_tokens=0,
+                  workspace=None, stream=None) -> None:
+    """Decode over E4M3 pools [N, Hkv, b, D] (uint8) with per-head scales;
+    q, out [B, Hq, D] in f16 or bf16."""
+    lib = load()
+    B, Hq, D = q.shape
+    N, Hkv, b, D2 = k_pool.shape
+    if D2 != D or tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype:
+        raise ValueError("shape mismatch between q, out and the pools")
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8 or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("FP8 pools are uint8 tensors [N, Hkv, b, D]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    ws_ptr, ws_bytes = C.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib.pa_decode_fp8(_dev(out, "out", q.dtype), _dev(q, "q", q.dtype), _dtype_id(q), _dev(k_pool, "k_pool"),
+                            _dev(v_pool, "v_pool"), _dev(k_scale, "k_scale", torch.float32),
+                            _dev(v_scale, "v_scale", torch.float32), N,
+                            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                            _dev(seq_lens, "seq_lens", torch.int32), B, Hq, Hkv, D, b, float(scale),
+                            int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)), "pa_decode_fp8")
 
 
 DECODE_KERNELS = {"auto": 0, "simt": 1, "mma": 2}

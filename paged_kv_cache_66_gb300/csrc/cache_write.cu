@@ -9,6 +9,8 @@
 // touch consecutive vectors of one row (append) or one block (copy), so every
 // warp access is a fully used, coalesced span, with several independent loads
 // in flight per thread before the stores.
+#include <cuda_fp8.h>
+
 #include "pa_common.cuh"
 #include "pa_launch.h"
 
@@ -113,6 +115,87 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(PoolPtrs pools, int nu
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (i0 + u * 256 < vec_per_block) d[i0 + u * 256] = x[u];
+}
+
+// FP8 append: the same scatter, quantising on the way.  Each thread turns 16
+// input elements of one (token, head) row of K or V into 16 E4M3 bytes:
+// code = e4m3(x / scale[h]) with an IEEE fp32 division, rounding to nearest
+// even and saturating to +-448 (cvt.rn.satfinite), then one 16-byte store.
+template <typename Tin>
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
+                                                            uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                                            const float* __restrict__ k_scale,
+                                                            const float* __restrict__ v_scale,
+                                                            const int64_t* __restrict__ slots, int rows,
+                                                            int64_t num_slots, int hkv, int vpr, int block_size,
+                                                            int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int total = rows * 2 * vpr;  // (row, K|V, 16-byte output chunk)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int c = i % vpr;
+        const int rk = i / vpr;
+        const int kind = rk & 1, r = rk >> 1;
+        const int t = r / hkv, h = r - t * hkv;
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (c == 0 && kind == 0 && h == 0) flag_error(err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / block_size, off = slot - blk * block_size;
+        const Tin* src = (kind == 0 ? k : v) + (static_cast<size_t>(r) * vpr + c) * 16;
+        const float sc = __ldg((kind == 0 ? k_scale : v_scale) + h);
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = Elt<Tin>::to_f32(src[4 * j]) / sc, b = Elt<Tin>::to_f32(src[4 * j + 1]) / sc;
+            const float cc = Elt<Tin>::to_f32(src[4 * j + 2]) / sc, d = Elt<Tin>::to_f32(src[4 * j + 3]) / sc;
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(cc, d), __NV_SATFINITE, __NV_E4M3);
+            w[j] = (lo & 0xFFFFu) | (hi << 16);
+        }
+        const size_t dst = ((static_cast<size_t>(blk) * hkv + h) * block_size + off) * vpr + c;
+        (kind == 0 ? k_pool : v_pool)[dst] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+cudaError_t launch_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,
+                                 const float* k_scale, const float* v_scale, const int64_t* slots,
+                                 int64_t num_tokens, int64_t num_blocks, int hkv, int d, int block_size, int* err,
+                                 cudaStream_t stream) {
+    const int vpr = d / 16;  // 16-byte output chunks per row
+    const int64_t chunk = ((1LL << 29) / (hkv * 2LL * vpr)) > 0 ? ((1LL << 29) / (hkv * 2LL * vpr)) : 1;
+    const int es = in_dtype == PA_F32 ? 4 : 2;
+    for (int64_t t0 = 0; t0 < num_tokens; t0 += chunk) {
+        const int64_t nt = (num_tokens - t0 < chunk) ? (num_tokens - t0) : chunk;
+        const int rows = static_cast<int>(nt * hkv);
+        int64_t blocks = (static_cast<int64_t>(rows) * 2 * vpr + 255) / 256;
+        if (blocks > 152LL * 12) blocks = 152LL * 12;
+        if (blocks < 1) blocks = 1;
+        const size_t off = static_cast<size_t>(t0) * hkv * d * es;
+        const char* kb = static_cast<const char*>(k) + off;
+        const char* vb = static_cast<const char*>(v) + off;
+        cudaError_t e;
+        const int64_t ns = num_blocks * block_size;
+        uint4* kp = static_cast<uint4*>(k_pool);
+        uint4* vp = static_cast<uint4*>(v_pool);
+        dim3 grid(static_cast<unsigned>(blocks)), block(256);
+        if (in_dtype == PA_F16)
+            e = launch_pdl(kv_append_fp8_kernel<__half>, grid, block, 0, stream, reinterpret_cast<const __half*>(kb),
+                           reinterpret_cast<const __half*>(vb), kp, vp, k_scale, v_scale, slots + t0, rows, ns, hkv,
+                           vpr, block_size, err);
+        else if (in_dtype == PA_BF16)
+            e = launch_pdl(kv_append_fp8_kernel<__nv_bfloat16>, grid, block, 0, stream,
+                           reinterpret_cast<const __nv_bfloat16*>(kb), reinterpret_cast<const __nv_bfloat16*>(vb), kp,
+                           vp, k_scale, v_scale, slots + t0, rows, ns, hkv, vpr, block_size, err);
+        else
+            e = launch_pdl(kv_append_fp8_kernel<float>, grid, block, 0, stream, reinterpret_cast<const float*>(kb),
+                           reinterpret_cast<const float*>(vb), kp, vp, k_scale, v_scale, slots + t0, rows, ns, hkv,
+                           vpr, block_size, err);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Failure-path check of the bounded waits: one warp initialises an mbarrier

@@ -19,9 +19,9 @@ cudaError_t launch_decode_path(const DecodeParams& p, cudaStream_t stream) {
         const uint64_t rows = static_cast<uint64_t>(p.num_blocks) * p.hkv * p.block_size;
         if (p.kernel != PA_DECODE_SIMT && rows < (1ull << 31)) {
             CUtensorMap km, vm;
-            if (!encode_pool_tmap(&km, p.k_pool, rows, D) || !encode_pool_tmap(&vm, p.v_pool, rows, D))
+            if (!encode_pool_tmap(&km, p.k_pool, rows, D, 2) || !encode_pool_tmap(&vm, p.v_pool, rows, D, 2))
                 return cudaErrorInvalidValue;
-            return launch_mma<T, D, G>(p, km, vm, stream);
+            return launch_mma<T, T, D, G>(p, km, vm, stream);
         }
         if (p.kernel == PA_DECODE_MMA) return cudaErrorNotSupported;
     } else {
@@ -47,6 +47,36 @@ cudaError_t dispatch_decode(const DecodeParams& p, cudaStream_t stream) {
         case 64: return dispatch_group<T, 64>(p, stream);
         case 128: return dispatch_group<T, 128>(p, stream);
         case 256: return dispatch_group<T, 256>(p, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace pa
+
+namespace pa {
+
+// FP8 (E4M3) pools: the tensor-core kernel with byte tiles; D a multiple of 128.
+template <typename T, int D>
+cudaError_t dispatch_fp8_group(const DecodeParams& p, cudaStream_t stream) {
+    const uint64_t rows = static_cast<uint64_t>(p.num_blocks) * p.hkv * p.block_size;
+    if (rows >= (1ull << 31)) return cudaErrorNotSupported;
+    CUtensorMap km, vm;
+    if (!encode_pool_tmap(&km, p.k_pool, rows, D, 1) || !encode_pool_tmap(&vm, p.v_pool, rows, D, 1))
+        return cudaErrorInvalidValue;
+    switch (p.hq / p.hkv) {
+        case 1: return launch_mma<T, uint8_t, D, 1>(p, km, vm, stream);
+        case 2: return launch_mma<T, uint8_t, D, 2>(p, km, vm, stream);
+        case 4: return launch_mma<T, uint8_t, D, 4>(p, km, vm, stream);
+        case 8: return launch_mma<T, uint8_t, D, 8>(p, km, vm, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+template <typename T>
+cudaError_t dispatch_decode_fp8(const DecodeParams& p, cudaStream_t stream) {
+    switch (p.d) {
+        case 128: return dispatch_fp8_group<T, 128>(p, stream);
+        case 256: return dispatch_fp8_group<T, 256>(p, stream);
         default: return cudaErrorNotSupported;
     }
 }

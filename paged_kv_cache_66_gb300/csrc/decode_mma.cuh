@@ -21,9 +21,25 @@
 // swizzle, so the ldmatrix reads of the fragments are bank-conflict free.
 // Each warp owns every NW-th tile of the partition and a STAGES-deep ring,
 // lane 0 issuing the tensor copies STAGES tiles ahead on per-stage mbarriers.
+//
+// FP8 (E4M3) pools, with one fp32 scale per KV head for K and for V, run the
+// same kernel with P = uint8_t: a 128-byte TMA box holds 128 dims, ldmatrix
+// moves byte pairs, and cvt.e4m3x2 turns them into f16 operands (exact).  For
+// the scores, one ldmatrix of 8 tokens x 16 bytes gives lane (g, t) dims
+// 4t..4t+3 of token g; these serve as k = {2t, 2t+1} and {2t+8, 2t+9} of the
+// MMA, and q's fragment is loaded with the same permutation (a dot product is
+// indifferent to the order of its terms).  For the output, the transposed
+// load gives lane (g, t) dims {2g, 2g+1} of tokens {2t, 2t+1}; after a byte
+// select, MMA row g stands for dim 2g and row g+8 for dim 2g+1, which the
+// write-out undoes.  q is used in f16 (exact for bf16 inputs in f16's normal
+// range), the K scale folds into the score scale, the V scale into the
+// partial outputs.
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "decode_merge.cuh"
 #include "pa_common.cuh"
@@ -94,18 +110,37 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// two E4M3 codes (low byte first) -> f16x2 (exact)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t to_h2(T a, T b) {
+    return pack2<__half>(Elt<T>::to_f32(a), Elt<T>::to_f32(b));
+}
+
 // ------------------------------------------------------------------ configuration
-template <typename T, int D, int G>
+// P = pool element: the 16-bit type of q, or uint8_t (E4M3) with a 16-bit q.
+template <typename P, int D, int G>
 struct MmaCfg {
-    static_assert(sizeof(T) == 2, "tensor-core path is for 16-bit pools");
+    static constexpr int EB = static_cast<int>(sizeof(P));
+    static_assert(EB == 2 || EB == 1, "16-bit or FP8 pools");
+    static constexpr bool F8 = EB == 1;
     static constexpr int TILE = 16;                    // tokens per tile (M of the score MMA)
-    static constexpr int NBOX = D / 64;                // 128-byte boxes per 16-token row block
+    static constexpr int ROW_BYTES = D * EB;
+    static_assert(ROW_BYTES % 128 == 0, "rows of whole 128-byte boxes");
+    static constexpr int NBOX = ROW_BYTES / 128;       // 128-byte boxes per 16-token row block
+    static constexpr int BOX_ELEMS = 128 / EB;
+    static constexpr int CHUNKS = ROW_BYTES / 16;      // 16-byte chunks per row
     static constexpr int BOX_BYTES = TILE * 128;       // 2 KiB, 1024-byte aligned in smem
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
-    // 2 stages x 4 warps (2 warps for D = 256): 32-64 KiB per CTA, so 3+ CTAs
-    // share an SM; deeper rings measured slower on the long-context workload
-    // (fewer resident CTAs to cover each CTA's start and end).
+    // 2 stages x 4 warps (2 warps when a stage is >= 16 KiB; 4 stages for the
+    // 4 KiB stages of FP8 at D = 128): 32-64 KiB per CTA, so 3+ CTAs share an
+    // SM; deeper rings measured slower on the long-context workload (fewer
+    // resident CTAs to cover each CTA's start and end).
 #ifdef PA_MMA_WARPS
     static constexpr int NW = PA_MMA_WARPS;  // build-time override (tuning sweeps)
 #else
@@ -114,7 +149,7 @@ struct MmaCfg {
 #ifdef PA_MMA_STAGES
     static constexpr int STAGES = PA_MMA_STAGES;
 #else
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = (F8 && STAGE_BYTES <= 4096) ? 4 : 2;
 #endif
     static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_BYTES;
@@ -123,6 +158,7 @@ struct MmaCfg {
     static constexpr int RED_BYTES = NW * G * (D + 2) * 4;
     static_assert(RED_BYTES <= RING_BYTES, "merge scratch aliases the ring");
     static_assert(G >= 1 && G <= 8, "query group on the N = 8 side");
+    static_assert(!F8 || KSTEPS % 2 == 0, "FP8 fragments come in pairs of k-steps");
     // + 1 KiB so the ring can be aligned to 1024 bytes for the 128-byte swizzle
     static constexpr size_t smem_bytes(int table_entries) {
         return 1024 + static_cast<size_t>(TBL_OFF) + static_cast<size_t>(table_entries) * 4;
@@ -135,12 +171,14 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
+template <typename T, typename PE, int D, int G>
+__global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
     decode_partition_mma(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
-    using C = MmaCfg<T, D, G>;
+    using C = MmaCfg<PE, D, G>;
     constexpr int NW = C::NW, STAGES = C::STAGES, KSTEPS = C::KSTEPS;
+    constexpr bool F8 = C::F8;
+    using TM = std::conditional_t<F8, __half, T>;  // MMA operand type
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
         smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-byte aligned ring
@@ -202,8 +240,8 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
         mbar_arrive_expect_tx(&bars[st], 2 * C::TILE_BYTES);
 #pragma unroll
         for (int bx = 0; bx < C::NBOX; ++bx) {
-            tma_load_2d(dst + bx * C::BOX_BYTES, &kmap, bx * 64, row, &bars[st]);
-            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &vmap, bx * 64, row, &bars[st]);
+            tma_load_2d(dst + bx * C::BOX_BYTES, &kmap, bx * C::BOX_ELEMS, row, &bars[st]);
+            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &vmap, bx * C::BOX_ELEMS, row, &bars[st]);
         }
     };
     if (lane == 0)
@@ -218,8 +256,15 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
             if (g < G) {
-                qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 2 * t));
-                qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + 2 * t));
+                if constexpr (F8) {
+                    // dims 4t..4t+3 of this 16-dim step, matching the K fragment below
+                    const T* q4 = qrow + ks * 16 + 4 * t;
+                    qb[ks][0] = to_h2<T>(q4[0], q4[1]);
+                    qb[ks][1] = to_h2<T>(q4[2], q4[3]);
+                } else {
+                    qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 2 * t));
+                    qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + 2 * t));
+                }
             } else {
                 qb[ks][0] = 0u;
                 qb[ks][1] = 0u;
@@ -232,7 +277,7 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const float sl2 = p.scale_log2;
+    const float sl2 = F8 ? p.scale_log2 * __ldg(p.k_scale + kvh) : p.scale_log2;
 
     // ldmatrix addressing: lane provides row (lane & 7) of matrix (lane >> 3)
     const int lm = lane >> 3, lr = lane & 7;
@@ -254,11 +299,25 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
             const uint32_t kbase = smem_u32(kt);
             const int krow = lr + (lm & 1) * 8;
+            if constexpr (F8) {
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(kbase + swz(krow, ks * 2 + (lm >> 1)), a);
-                mma16816<T>(sc, a, qb[ks][0], qb[ks][1]);
+                for (int ks = 0; ks < KSTEPS; ks += 2) {
+                    uint32_t r[4];
+                    ldsm_x4(kbase + swz(lr + (lm & 1) * 8, ks + (lm >> 1)), r);
+                    const uint32_t a0[4] = {e4m3x2_to_h2(r[0]), e4m3x2_to_h2(r[1]), e4m3x2_to_h2(r[0] >> 16),
+                                            e4m3x2_to_h2(r[1] >> 16)};
+                    const uint32_t a1[4] = {e4m3x2_to_h2(r[2]), e4m3x2_to_h2(r[3]), e4m3x2_to_h2(r[2] >> 16),
+                                            e4m3x2_to_h2(r[3] >> 16)};
+                    mma16816<TM>(sc, a0, qb[ks][0], qb[ks][1]);
+                    mma16816<TM>(sc, a1, qb[ks + 1][0], qb[ks + 1][1]);
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    uint32_t a[4];
+                    ldsm_x4(kbase + swz(krow, ks * 2 + (lm >> 1)), a);
+                    mma16816<TM>(sc, a, qb[ks][0], qb[ks][1]);
+                }
             }
             // sc = {S[tok g][h0], S[tok g][h1], S[tok g+8][h0], S[tok g+8][h1]}
             const bool v0 = g < nv, v1 = g + 8 < nv;
@@ -297,12 +356,12 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
             l0 += p0 + p2;
             l1 += p1 + p3;
             // P^T operand: transpose the 8x8 (token x head) halves
-            const uint32_t pb0 = movmatrix_t(pack2<T>(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack2<T>(p2, p3));
+            const uint32_t pb0 = movmatrix_t(pack2<TM>(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack2<TM>(p2, p3));
             if (nv < C::TILE) {
                 // unwritten slots of the tail may hold anything (NaN * 0 = NaN): zero those V rows
-                for (int e = lane; e < (C::TILE - nv) * (D / 8); e += 32) {
-                    const int r = nv + e / (D / 8), c = e % (D / 8);
+                for (int e = lane; e < (C::TILE - nv) * C::CHUNKS; e += 32) {
+                    const int r = nv + e / C::CHUNKS, c = e % C::CHUNKS;
                     *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 __syncwarp();
@@ -310,11 +369,30 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
             // ---- O^T += V^T P^T
             const uint32_t vbase = smem_u32(vt);
             const int vrow = lr + (lm >> 1) * 8;
+            if constexpr (F8) {
 #pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt) {
-                uint32_t a[4];
-                ldsm_x4_t(vbase + swz(vrow, mt * 2 + (lm & 1)), a);
-                mma16816<T>(acc[mt], a, pb0, pb1);
+                for (int mt = 0; mt < KSTEPS; mt += 2) {
+                    uint32_t r[4];
+                    ldsm_x4_t(vbase + swz(lr + (lm & 1) * 8, mt + (lm >> 1)), r);
+                    // r[i] bytes: (tok 2t, dim 2g), (tok 2t, dim 2g+1), (tok 2t+1, dim 2g), (tok 2t+1, dim 2g+1)
+                    const uint32_t a0[4] = {e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x20u)),
+                                            e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x31u)),
+                                            e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x20u)),
+                                            e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x31u))};
+                    const uint32_t a1[4] = {e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x20u)),
+                                            e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x31u)),
+                                            e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x20u)),
+                                            e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x31u))};
+                    mma16816<TM>(acc[mt], a0, pb0, pb1);
+                    mma16816<TM>(acc[mt + 1], a1, pb0, pb1);
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    uint32_t a[4];
+                    ldsm_x4_t(vbase + swz(vrow, mt * 2 + (lm & 1)), a);
+                    mma16816<TM>(acc[mt], a, pb0, pb1);
+                }
             }
         }
         __syncwarp();
@@ -349,16 +427,18 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
             red_l[warp * G + h1] = l1;
         }
     }
+    // MMA rows g and g+8 are dims g and g+8 of the 16-dim tile (FP8: dims 2g, 2g+1)
+    const int dA = F8 ? 2 * g : g, dB = F8 ? 2 * g + 1 : g + 8;
+    const float vs = F8 ? __ldg(p.v_scale + kvh) : 1.f;
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) {
-        const int d0 = mt * 16 + g;
         if (h0 < G) {
-            red_acc[(warp * G + h0) * D + d0] = acc[mt][0];
-            red_acc[(warp * G + h0) * D + d0 + 8] = acc[mt][2];
+            red_acc[(warp * G + h0) * D + mt * 16 + dA] = acc[mt][0] * vs;
+            red_acc[(warp * G + h0) * D + mt * 16 + dB] = acc[mt][2] * vs;
         }
         if (h1 < G) {
-            red_acc[(warp * G + h1) * D + d0] = acc[mt][1];
-            red_acc[(warp * G + h1) * D + d0 + 8] = acc[mt][3];
+            red_acc[(warp * G + h1) * D + mt * 16 + dA] = acc[mt][1] * vs;
+            red_acc[(warp * G + h1) * D + mt * 16 + dB] = acc[mt][3] * vs;
         }
     }
     __syncthreads();
@@ -392,23 +472,24 @@ __global__ void __launch_bounds__(MmaCfg<T, D, G>::NW * 32)
 
 }
 
-template <typename T, int D, int G>
+template <typename T, typename PE, int D, int G>
 cudaError_t launch_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        cudaStream_t stream) {
-    using C = MmaCfg<T, D, G>;
+    using C = MmaCfg<PE, D, G>;
     const size_t smem = C::smem_bytes(p.partition_tokens / p.block_size);
     static int configured_for = -1;  // device on which the attribute was last set
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        cudaError_t e = cudaFuncSetAttribute(decode_partition_mma<T, D, G>,
+        cudaError_t e = cudaFuncSetAttribute(decode_partition_mma<T, PE, D, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(C::smem_bytes(8192 / 16)));
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     dim3 grid(p.max_partitions, p.hkv, p.batch);
-    cudaError_t e = launch_pdl(decode_partition_mma<T, D, G>, grid, dim3(C::NW * 32), smem, stream, p, kmap, vmap);
+    cudaError_t e =
+        launch_pdl(decode_partition_mma<T, PE, D, G>, grid, dim3(C::NW * 32), smem, stream, p, kmap, vmap);
     if (e != cudaSuccess || p.max_partitions <= 1) return e;
     return launch_merge<T, D>(p, stream);
 }

@@ -83,7 +83,7 @@ WsLayout ws_layout(int batch, int hq, int d, int max_blocks, int b, int part) {
 
 namespace pa {
 
-bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d) {
+bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q{};
@@ -94,10 +94,10 @@ bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d) 
     });
     if (!g_encode) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    const cuuint32_t box[2] = {64, 16};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * elt_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt_bytes), 16};
     const cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+    return g_encode(map, elt_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -217,6 +217,82 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
         case PA_BF16: return from_cuda(pa::launch_decode_bf16(p, st));
         default: return PA_ERR_INVALID;
     }
+}
+
+pa_status pa_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,
+                           const float* k_scale, const float* v_scale, const int64_t* slot_mapping,
+                           int64_t num_tokens, int64_t num_blocks, int num_kv_heads, int head_dim, int block_size,
+                           void* stream) {
+    if (elt_size(in_dtype) == 0 || num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0)
+        return PA_ERR_INVALID;
+    if (!k_pool || !v_pool || !al(k_pool, 16) || !al(v_pool, 16)) return PA_ERR_INVALID;
+    if (head_dim % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_scale || !v_scale || !slot_mapping || !al(k, 16) || !al(v, 16) || !al(slot_mapping, 8) ||
+        !al(k_scale, 4) || !al(v_scale, 4))
+        return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    return from_cuda(pa::launch_kv_append_fp8(k, v, in_dtype, k_pool, v_pool, k_scale, v_scale, slot_mapping,
+                                              num_tokens, num_blocks, num_kv_heads, head_dim, block_size, err,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* k_pool, const void* v_pool,
+                        const float* k_scale, const float* v_scale, int64_t num_blocks, const int32_t* block_tables,
+                        int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                        int head_dim, int block_size, float scale, int partition_tokens, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if ((q_dtype != PA_F16 && q_dtype != PA_BF16) || batch < 0 || batch > 65535 || num_q_heads <= 0 ||
+        num_kv_heads <= 0 || num_kv_heads > 65535 || head_dim <= 0 || block_size <= 0 || max_blocks <= 0 ||
+        num_blocks <= 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
+    if (static_cast<uint64_t>(num_blocks) * num_kv_heads * block_size >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
+    const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    if (part <= 0 || part > kMaxPartition || part % 16 != 0 || part % block_size != 0) return PA_ERR_INVALID;
+    if (static_cast<int64_t>(max_blocks) * block_size > (1LL << 30)) return PA_ERR_INVALID;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !k_scale || !v_scale || !block_tables || !seq_lens) return PA_ERR_INVALID;
+    if (!al(out, 16) || !al(q, 16) || !al(k_pool, 16) || !al(v_pool, 16) || !al(block_tables, 4) ||
+        !al(seq_lens, 4) || !al(k_scale, 4) || !al(v_scale, 4))
+        return PA_ERR_INVALID;
+    const WsLayout ws = ws_layout(batch, num_q_heads, head_dim, max_blocks, block_size, part);
+    if (ws.partitions > 1 && (!workspace || !al(workspace, 16) || workspace_bytes < ws.total))
+        return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    pa::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    char* wsb = static_cast<char*>(workspace);
+    p.ws_ml = ws.partitions > 1 ? reinterpret_cast<float*>(wsb) : nullptr;
+    p.ws_acc = ws.partitions > 1 ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks;
+    p.batch = batch;
+    p.hq = num_q_heads;
+    p.hkv = num_kv_heads;
+    p.d = head_dim;
+    p.block_size = block_size;
+    p.partition_tokens = part;
+    p.max_partitions = ws.partitions < 1 ? 1 : ws.partitions;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kernel = PA_DECODE_MMA;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return from_cuda(q_dtype == PA_F16 ? pa::launch_decode_fp8_f16(p, st) : pa::launch_decode_fp8_bf16(p, st));
 }
 
 pa_status pa_selftest_wait_timeout(int limit_us, void* stream) {

@@ -37,6 +37,8 @@ struct DecodeParams {
     int max_partitions;         // P = ceil(max_blocks * b / partition_tokens)
     float scale_log2;           // scale * log2(e)
     int kernel;                 // pa_decode_kernel choice (PA_DECODE_AUTO / _SIMT / _MMA)
+    const float* k_scale;       // FP8 pools: [Hkv] scale of K codes (else null)
+    const float* v_scale;       // FP8 pools: [Hkv] scale of V codes (else null)
 };
 
 // Launch `kernel` on `stream` allowing programmatic dependent launch (the
@@ -57,9 +59,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// 2-D TMA descriptor of a pool viewed as [rows, D] 16-bit elements, boxes of
-// 16 rows x 64 elements (128 bytes) with the 128-byte swizzle.
-bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d);
+// 2-D TMA descriptor of a pool viewed as [rows, D] elements of `elt_bytes`
+// (2, or 1 for FP8), boxes of 16 rows x 128 bytes with the 128-byte swizzle.
+bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes);
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slots,
                              int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,
@@ -74,5 +76,13 @@ cudaError_t launch_copy_blocks(const PoolPtrs& pools, int num_layers, const int6
 cudaError_t launch_decode_f32(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_f16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
+// FP8 (E4M3) pools; q / out in f16 or bf16.
+cudaError_t launch_decode_fp8_f16(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_fp8_bf16(const DecodeParams& p, cudaStream_t stream);
+
+cudaError_t launch_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,
+                                 const float* k_scale, const float* v_scale, const int64_t* slots,
+                                 int64_t num_tokens, int64_t num_blocks, int hkv, int d, int block_size, int* err,
+                                 cudaStream_t stream);
 
 }  // namespace pa

@@ -62,17 +62,48 @@ class DeviceStep:
 
 
 class Replay:
-    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None):
+    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None, kv="native"):
+        """kv = "native": pools in the workload's dtype; kv = "fp8": E4M3 pools
+        with the workload's per-(layer, KV head) scales."""
         self.wl = wl
         self.device = torch.device(device)
         self.layers = list(range(wl.layers)) if layers is None else list(layers)
         self.host = HostBlockManager(wl.num_blocks, wl.b, wl.free_order)
+        self.kv = kv
         shape = (wl.num_blocks, wl.Hkv, wl.b, wl.D)
-        self.k_pools = [torch.zeros(shape, dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
-        self.v_pools = [torch.zeros(shape, dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
+        pool_dtype = torch.uint8 if kv == "fp8" else wl.torch_dtype
+        self.k_pools = [torch.zeros(shape, dtype=pool_dtype, device=self.device) for _ in self.layers]
+        self.v_pools = [torch.zeros(shape, dtype=pool_dtype, device=self.device) for _ in self.layers]
+        if kv == "fp8":
+            self.k_scales = [torch.as_tensor(wcfg.kv_scales(wl, layer, "k")).to(self.device) for layer in self.layers]
+            self.v_scales = [torch.as_tensor(wcfg.kv_scales(wl, layer, "v")).to(self.device) for layer in self.layers]
         self.partition_tokens = wl.partition_tokens if partition_tokens is None else partition_tokens
         self.steps_done = 0
         self._ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+
+    @property
+    def kv_elt(self) -> int:
+        """Bytes per stored K/V element."""
+        return 1 if self.kv == "fp8" else self.wl.elt
+
+    def append(self, li: int, k, v, slots, stream=None):
+        """pa_kv_append (or its FP8 form) into layer slot li."""
+        if self.kv == "fp8":
+            api.pa_kv_append_fp8(k, v, self.k_pools[li], self.v_pools[li], self.k_scales[li], self.v_scales[li],
+                                 slots, stream=stream)
+        else:
+            api.pa_kv_append(k, v, self.k_pools[li], self.v_pools[li], slots, stream=stream)
+
+    def decode(self, li: int, out, q, tables, lens, workspace, stream=None):
+        """pa_decode (or its FP8 form) over layer slot li."""
+        ws = workspace if workspace is not None and workspace.numel() else None
+        if self.kv == "fp8":
+            api.pa_decode_fp8(out, q, self.k_pools[li], self.v_pools[li], self.k_scales[li], self.v_scales[li],
+                              tables, lens, self.wl.scale, partition_tokens=self.partition_tokens, workspace=ws,
+                              stream=stream)
+        else:
+            api.pa_decode(out, q, self.k_pools[li], self.v_pools[li], tables, lens, self.wl.scale,
+                          partition_tokens=self.partition_tokens, workspace=ws, stream=stream)
 
     # ------------------------------------------------------------------ ops
     def _copy(self, pairs: np.ndarray):
@@ -102,7 +133,7 @@ class Replay:
                 c1 = min(n, c0 + chunk)
                 k = wcfg.kv_rows(wl, layer, "k", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
                 v = wcfg.kv_rows(wl, layer, "v", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
-                api.pa_kv_append(k, v, self.k_pools[li], self.v_pools[li], slots_d[c0:c1], stream=stream)
+                self.append(li, k, v, slots_d[c0:c1], stream=stream)
 
     def _write(self, uid: int, n: int):
         self._write_device(self._write_host(uid, n))
@@ -194,9 +225,6 @@ class Replay:
         if outs is None:
             outs = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
         for li in range(len(self.layers)):
-            api.pa_kv_append(ds.k_new[li], ds.v_new[li], self.k_pools[li], self.v_pools[li], ds.slots,
-                             stream=stream)
-            api.pa_decode(outs[li], ds.q[li], self.k_pools[li], self.v_pools[li], ds.tables, ds.lens, wl.scale,
-                          partition_tokens=self.partition_tokens, workspace=ws if ws.numel() else None,
-                          stream=stream)
+            self.append(li, ds.k_new[li], ds.v_new[li], ds.slots, stream=stream)
+            self.decode(li, outs[li], ds.q[li], ds.tables, ds.lens, ws, stream=stream)
         return outs

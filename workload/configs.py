@@ -108,6 +108,14 @@ def kv_rows(wl: Workload, layer: int, kind: str, owners, positions, heads=None,
     return rng.normal_from_index(key, idx).to(wl.torch_dtype)
 
 
+def kv_scales(wl: Workload, layer: int, kind: str) -> np.ndarray:
+    """fp32 [Hkv] scales of an FP8 (E4M3) K or V pool: 1/32, spread slightly by
+    head and layer (values of about N(0, 1) then use codes up to ~110 of 448)."""
+    h = np.arange(wl.Hkv, dtype=np.float64)
+    base = 1.0 / 32 if kind == "k" else 1.0 / 30
+    return (base * (1.0 + 0.05 * h + 0.01 * layer)).astype(np.float32)
+
+
 def q_rows(wl: Workload, layer: int, step: int, rows, device="cpu") -> torch.Tensor:
     """Query rows [len(rows), Hq, D] for decode step ``step`` in the storage dtype."""
     rows = torch.as_tensor(np.asarray(rows, dtype=np.int64), device=device)
