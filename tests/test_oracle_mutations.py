@@ -85,3 +85,26 @@ def test_lifo_free_list_is_caught(monkeypatch):
     monkeypatch.setattr(blocks.BlockAllocator, "allocate", lifo_allocate)
     with pytest.raises(AssertionError):
         pins.test_allocator_fifo_and_refcounts()
+
+
+def test_chain_without_parent_key_is_caught(monkeypatch):
+    """A key of the block's own tokens only lets equal text under another history match."""
+    from oracle import prefix_hash as ph
+    from tests import test_oracle_prefix_hash as hp
+    orig = ph.next_key
+    monkeypatch.setattr(ph, "next_key", lambda parent, toks: orig(b"", toks))
+    with pytest.raises(AssertionError):
+        hp.test_same_block_text_under_different_history_differs()
+    with pytest.raises(AssertionError):
+        hp.test_hash_table_equals_tuple_table_on_traces(0)
+
+
+def test_chain_without_salt_is_caught(monkeypatch):
+    from oracle import prefix_hash as ph
+    from tests import test_oracle_prefix_hash as hp
+    orig = ph.root_key
+    monkeypatch.setattr(ph, "root_key", lambda salt=b"": orig(b""))
+    with pytest.raises(AssertionError):
+        hp.test_salt_separates_every_key()
+    with pytest.raises(AssertionError):
+        hp.test_hash_table_equals_tuple_table_on_traces(0)
