@@ -106,6 +106,35 @@ pa_status pa_host_prefix_remember(pa_host* h, int64_t seq, const int64_t* tokens
 pa_status pa_host_prefix_evict(pa_host* h, int64_t blocks_wanted);
 int64_t pa_host_prefix_entries(const pa_host* h);
 
+/* Hash-chain prefix table ("Prefix caching": production engines hash the
+ * chain of block contents instead of keeping token tuples, and the key also
+ * covers whatever changes the activations: model revision, adapter,
+ * multimodal inputs).  Readings, since the pages fix no hash or layout:
+ *   root  = SHA-256("pagedkv.prefix.v1" || u64le(salt_len) || salt)
+ *   key_i = SHA-256(key_{i-1} || u32le(block_size) || i64le(token) for the
+ *           block_size tokens of full block i),  key_{-1} = root
+ * (SHA-256 of FIPS PUB 180-4).  `salt` is caller-owned bytes that identify
+ * everything besides the tokens that a block's K/V depend on; the same salt
+ * must be given to attach and remember.  attach / remember / evict follow the
+ * rules of the tuple-keyed table above; this table has its own entries and
+ * its own least-recently-used order, and the two tables never see each
+ * other's entries.  NULL handles or negative sizes give PA_ERR_INVALID. */
+
+/* Keys of the n / block_size full blocks of `tokens`: 32 bytes each, written
+ * to keys_out (caller-owned, (n / block_size) * 32 bytes). */
+pa_status pa_prefix_chain_keys(const int64_t* tokens, int64_t n, int block_size, const void* salt, int64_t salt_len,
+                               uint8_t* keys_out);
+pa_status pa_host_hprefix_attach(pa_host* h, int64_t seq, const int64_t* prompt, int64_t n, const void* salt,
+                                 int64_t salt_len, int64_t* reused);
+/* PA_ERR_INVALID when `seq` holds fewer than n / block_size blocks. */
+pa_status pa_host_hprefix_remember(pa_host* h, int64_t seq, const int64_t* tokens, int64_t n, const void* salt,
+                                   int64_t salt_len);
+pa_status pa_host_hprefix_evict(pa_host* h, int64_t blocks_wanted);
+int64_t pa_host_hprefix_entries(const pa_host* h);
+/* Cached block ids, least recently used first; writes at most `capacity`
+ * and returns the number of entries (-1 on invalid arguments). */
+int64_t pa_host_hprefix_blocks(const pa_host* h, int32_t* blocks_out, int64_t capacity);
+
 #ifdef __cplusplus
 }
 #endif

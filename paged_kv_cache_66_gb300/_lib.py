@@ -58,6 +58,12 @@ SIGNATURES = {
     "pa_host_prefix_remember": (_i32, [_vp, _i64, _p64, _i64]),
     "pa_host_prefix_evict": (_i32, [_vp, _i64]),
     "pa_host_prefix_entries": (_i64, [_vp]),
+    "pa_prefix_chain_keys": (_i32, [_p64, _i64, _i32, _vp, _i64, _vp]),
+    "pa_host_hprefix_attach": (_i32, [_vp, _i64, _p64, _i64, _vp, _i64, _p64]),
+    "pa_host_hprefix_remember": (_i32, [_vp, _i64, _p64, _i64, _vp, _i64]),
+    "pa_host_hprefix_evict": (_i32, [_vp, _i64]),
+    "pa_host_hprefix_entries": (_i64, [_vp]),
+    "pa_host_hprefix_blocks": (_i64, [_vp, _p32, _i64]),
 }
 
 _LIB = None

@@ -5,8 +5,8 @@
 // list plus refcounts), "The paged cache" (create / reserve / set_batch /
 // fork / free / truncate), "Sharing blocks: forks and copy-on-write" and
 // "Prefix caching".  Readings (first-in first-out free list, over-release
-// rejected before the decrement, all-or-nothing reserve) are stated in
-// include/pagedkv_host.h.
+// rejected before the decrement, all-or-nothing reserve, the byte layout of
+// the hash-chain prefix keys) are stated in include/pagedkv_host.h.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "../../include/pagedkv_host.h"
+#include "sha256.h"
 
 namespace {
 
@@ -36,6 +37,51 @@ struct VecHash {
     }
 };
 
+// A hash-chain prefix key (SHA-256 digest).
+struct ChainKey {
+    uint8_t b[32];
+    bool operator==(const ChainKey& o) const noexcept { return std::memcmp(b, o.b, 32) == 0; }
+};
+struct ChainKeyHash {
+    size_t operator()(const ChainKey& k) const noexcept {  // the key is already uniformly distributed
+        uint64_t x;
+        std::memcpy(&x, k.b, 8);
+        return static_cast<size_t>(x);
+    }
+};
+
+constexpr char kChainDomain[] = "pagedkv.prefix.v1";
+
+ChainKey chain_root(const void* salt, int64_t salt_len) {
+    pa_sha256::Hasher hs;
+    hs.update(kChainDomain, sizeof(kChainDomain) - 1);
+    uint8_t len[8];
+    for (int i = 0; i < 8; ++i) len[i] = static_cast<uint8_t>(static_cast<uint64_t>(salt_len) >> (8 * i));
+    hs.update(len, 8);
+    if (salt_len > 0) hs.update(salt, static_cast<size_t>(salt_len));
+    ChainKey k;
+    hs.finish(k.b);
+    return k;
+}
+
+// key of the next full block: the parent key, the block size (u32 LE) and
+// each token id (i64 LE)
+ChainKey chain_next(const ChainKey& parent, const int64_t* tokens, int block_size) {
+    pa_sha256::Hasher hs;
+    hs.update(parent.b, 32);
+    uint8_t buf[8];
+    for (int i = 0; i < 4; ++i) buf[i] = static_cast<uint8_t>(static_cast<uint32_t>(block_size) >> (8 * i));
+    hs.update(buf, 4);
+    for (int t = 0; t < block_size; ++t) {
+        const uint64_t x = static_cast<uint64_t>(tokens[t]);
+        for (int i = 0; i < 8; ++i) buf[i] = static_cast<uint8_t>(x >> (8 * i));
+        hs.update(buf, 8);
+    }
+    ChainKey k;
+    hs.finish(k.b);
+    return k;
+}
+
 }  // namespace
 
 struct pa_host {
@@ -49,6 +95,9 @@ struct pa_host {
     std::unordered_map<std::vector<int64_t>, std::pair<int32_t, std::list<std::vector<int64_t>>::iterator>,
                        VecHash>
         entries;
+    // hash-chain prefix table: chain key -> (block, position in its own LRU list)
+    std::list<ChainKey> hlru;
+    std::unordered_map<ChainKey, std::pair<int32_t, std::list<ChainKey>::iterator>, ChainKeyHash> hentries;
 
     int64_t blocks_needed(int64_t tokens) const { return (tokens + block_size - 1) / block_size; }
 
@@ -360,5 +409,91 @@ pa_status pa_host_prefix_evict(pa_host* h, int64_t blocks_wanted) {
 }
 
 int64_t pa_host_prefix_entries(const pa_host* h) { return h ? static_cast<int64_t>(h->entries.size()) : -1; }
+
+pa_status pa_prefix_chain_keys(const int64_t* tokens, int64_t n, int block_size, const void* salt, int64_t salt_len,
+                               uint8_t* keys_out) {
+    if (n < 0 || block_size <= 0 || salt_len < 0 || (n > 0 && !tokens) || (salt_len > 0 && !salt))
+        return PA_ERR_INVALID;
+    const int64_t full = n / block_size;
+    if (full > 0 && !keys_out) return PA_ERR_INVALID;
+    ChainKey k = chain_root(salt, salt_len);
+    for (int64_t i = 0; i < full; ++i) {
+        k = chain_next(k, tokens + i * block_size, block_size);
+        std::memcpy(keys_out + 32 * i, k.b, 32);
+    }
+    return PA_OK;
+}
+
+pa_status pa_host_hprefix_attach(pa_host* h, int64_t seq, const int64_t* prompt, int64_t n, const void* salt,
+                                 int64_t salt_len, int64_t* reused) {
+    if (!h || n < 0 || salt_len < 0 || (n > 0 && !prompt) || (salt_len > 0 && !salt)) return PA_ERR_INVALID;
+    if (h->seqs.count(seq)) return PA_ERR_EXISTS;
+    Seq s;
+    const int64_t size = h->block_size;
+    int64_t r = 0;
+    ChainKey k = chain_root(salt, salt_len);
+    while (r + size <= n - 1) {  // at least one prompt token is left to prefill
+        k = chain_next(k, prompt + r, h->block_size);
+        auto it = h->hentries.find(k);
+        if (it == h->hentries.end()) break;
+        h->hlru.splice(h->hlru.end(), h->hlru, it->second.second);  // most recently used
+        h->refs[it->second.first] += 1;
+        s.table.push_back(it->second.first);
+        r += size;
+    }
+    s.length = r;
+    h->seqs.emplace(seq, std::move(s));
+    if (reused) *reused = r;
+    return PA_OK;
+}
+
+pa_status pa_host_hprefix_remember(pa_host* h, int64_t seq, const int64_t* tokens, int64_t n, const void* salt,
+                                   int64_t salt_len) {
+    if (!h || n < 0 || salt_len < 0 || (n > 0 && !tokens) || (salt_len > 0 && !salt)) return PA_ERR_INVALID;
+    const Seq* s = h->find(seq);
+    if (!s) return PA_ERR_NOT_FOUND;
+    const int64_t size = h->block_size;
+    const int64_t full = n / size;
+    if (full > static_cast<int64_t>(s->table.size())) return PA_ERR_INVALID;
+    ChainKey k = chain_root(salt, salt_len);
+    for (int64_t i = 0; i < full; ++i) {
+        k = chain_next(k, tokens + i * size, h->block_size);
+        if (h->hentries.count(k)) continue;
+        const int32_t b = s->table[static_cast<size_t>(i)];
+        h->refs[b] += 1;
+        h->hlru.push_back(k);
+        h->hentries.emplace(k, std::make_pair(b, std::prev(h->hlru.end())));
+    }
+    return PA_OK;
+}
+
+pa_status pa_host_hprefix_evict(pa_host* h, int64_t blocks_wanted) {
+    if (!h) return PA_ERR_INVALID;
+    for (auto it = h->hlru.begin(); it != h->hlru.end();) {
+        if (static_cast<int64_t>(h->free_list.size()) >= blocks_wanted) break;
+        auto e = h->hentries.find(*it);
+        const int32_t b = e->second.first;
+        if (h->refs[b] == 1) {
+            h->hentries.erase(e);
+            it = h->hlru.erase(it);
+            h->release(b);
+        } else {
+            ++it;
+        }
+    }
+    return PA_OK;
+}
+
+int64_t pa_host_hprefix_entries(const pa_host* h) { return h ? static_cast<int64_t>(h->hentries.size()) : -1; }
+
+int64_t pa_host_hprefix_blocks(const pa_host* h, int32_t* blocks_out, int64_t capacity) {
+    if (!h || capacity < 0 || (capacity > 0 && !blocks_out)) return -1;
+    int64_t i = 0;
+    for (const ChainKey& k : h->hlru) {
+        if (i < capacity) blocks_out[i] = h->hentries.find(k)->second.first;
+        ++i;
+    }
+    return i;
+}
 
 }  // extern "C"

@@ -39,6 +39,28 @@ def _p32(a: np.ndarray):
     return a.ctypes.data_as(_P32)
 
 
+def prefix_salt(model_revision: str = "", adapter: str = "", extra=()) -> bytes:
+    """Salt bytes for the hash-chain prefix table: every field that changes a
+    block's K/V besides its tokens (model revision, adapter, multimodal input
+    digests), each length-prefixed so that no two field lists share bytes."""
+    out = bytearray()
+    for field in (model_revision, adapter, *extra):
+        b = field.encode() if isinstance(field, str) else bytes(field)
+        out += len(b).to_bytes(8, "little") + b
+    return bytes(out)
+
+
+def prefix_chain_keys(tokens, block_size: int, salt: bytes = b"") -> list:
+    """Hash-chain keys (32 bytes each) of the full blocks of ``tokens``."""
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    full = t.shape[0] // int(block_size) if int(block_size) > 0 else 0   # the library rejects block_size <= 0
+    out = np.zeros(max(full, 1) * 32, dtype=np.uint8)
+    salt = bytes(salt)
+    _raise(load().pa_prefix_chain_keys(_p64(t), t.shape[0], int(block_size), salt, len(salt),
+                                       out.ctypes.data_as(C.c_void_p)), "chain keys")
+    return [out[32 * i:32 * (i + 1)].tobytes() for i in range(full)]
+
+
 class HostBlockManager:
     """Free list + refcounts, per-sequence block tables, prefix table (C++)."""
 
@@ -160,3 +182,32 @@ class HostBlockManager:
     @property
     def prefix_entries(self) -> int:
         return int(self._lib.pa_host_prefix_entries(self._h))
+
+    # ------------------------------------------------ hash-chain prefix table
+    def hprefix_attach(self, seq: int, prompt, salt: bytes = b"") -> int:
+        p = np.ascontiguousarray(np.asarray(prompt, dtype=np.int64))
+        out = np.zeros(1, dtype=np.int64)
+        salt = bytes(salt)
+        _raise(self._lib.pa_host_hprefix_attach(self._h, int(seq), _p64(p), p.shape[0], salt, len(salt), _p64(out)),
+               "attach")
+        return int(out[0])
+
+    def hprefix_remember(self, seq: int, tokens, salt: bytes = b"") -> None:
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        salt = bytes(salt)
+        _raise(self._lib.pa_host_hprefix_remember(self._h, int(seq), _p64(t), t.shape[0], salt, len(salt)),
+               "remember")
+
+    def hprefix_evict(self, blocks_wanted: int) -> None:
+        _raise(self._lib.pa_host_hprefix_evict(self._h, int(blocks_wanted)), "evict")
+
+    @property
+    def hprefix_entries(self) -> int:
+        return int(self._lib.pa_host_hprefix_entries(self._h))
+
+    def hprefix_blocks(self) -> list:
+        """Cached block ids, least recently used first."""
+        n = int(self._lib.pa_host_hprefix_blocks(self._h, None, 0))
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._lib.pa_host_hprefix_blocks(self._h, _p32(out), n)
+        return out[:n].tolist()
