@@ -108,3 +108,41 @@ def test_chain_without_salt_is_caught(monkeypatch):
         hp.test_salt_separates_every_key()
     with pytest.raises(AssertionError):
         hp.test_hash_table_equals_tuple_table_on_traces(0)
+
+
+def _prefill_off_by_one(q, K, V, scale):
+    """Causal bound p < i instead of p <= i (the first row then sees nothing)."""
+    q = np.asarray(q, dtype=np.float64)
+    C, L = q.shape[0], K.shape[0]
+    out = np.zeros(q.shape)
+    for r in range(C):
+        out[r] = attention.decode_attention(q[r], K[:L - C + r], V[:L - C + r], scale)
+    return out
+
+
+def _prefill_no_mask(q, K, V, scale):
+    q = np.asarray(q, dtype=np.float64)
+    return np.stack([attention.decode_attention(q[r], K, V, scale) for r in range(q.shape[0])])
+
+
+def _prefill_chunk_at_start(q, K, V, scale):
+    """Chunk rows placed at positions 0 .. C-1 instead of the last C positions."""
+    q = np.asarray(q, dtype=np.float64)
+    return np.stack([attention.decode_attention(q[r], K[:r + 1], V[:r + 1], scale) for r in range(q.shape[0])])
+
+
+@pytest.mark.parametrize("bad", [_prefill_off_by_one, _prefill_no_mask, _prefill_chunk_at_start])
+def test_prefill_mistakes_are_caught(monkeypatch, bad):
+    from oracle import prefill
+    from tests import test_oracle_prefill as pp
+    monkeypatch.setattr(prefill, "prefill_attention", bad)
+    caught = 0
+    for test in (lambda: pp.test_full_prefill_matches_library_causal_sdpa(4, 2, 8, 37),
+                 pp.test_first_position_sees_only_v0_and_constant_keys_give_running_mean,
+                 pp.test_chunk_of_one_row_is_decode,
+                 lambda: pp.test_chunk_rows_equal_rows_of_the_whole_prefill(5)):
+        try:
+            test()
+        except AssertionError:
+            caught += 1
+    assert caught >= 1
