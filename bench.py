@@ -80,6 +80,16 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Dense 16-bit tensor peak for a kernel timed alone: the measured cuBLAS bf16
+    burst figure (fp16 runs at the same nominal rate)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except Exception:
+        return 1900.0, "fallback bf16 burst"
+
+
 def _kernel_sha() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -261,7 +271,7 @@ def run_ours(args, ws, rank, local):
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
         wl.layers = min(wl.layers, args.layers)
-    rp = Replay(wl, device=dev, kv=args.kv)
+    rp = Replay(wl, device=dev, kv=args.kv, partition_tokens=args.partition or None)
     rp.run_setup()
     torch.cuda.synchronize()
 
@@ -438,7 +448,8 @@ def run_op(args, local):
     line): "append" = pa_kv_append of 8 x 4096 new tokens into a long-context
     pool; "copy" = pa_copy_blocks of 64 copy-on-write pairs over 32 layers;
     "host" = the C++ plan of one decode step (pa_host_decode_step) for the
-    long-context and prefix-shared batches."""
+    long-context and prefix-shared batches; "prefill" = pa_prefill of 8 chunks of
+    1024 tokens over 3072 cached tokens each (Llama-3-8B-shaped layer)."""
     from paged_kv_cache_66_gb300 import api
     from paged_kv_cache_66_gb300.host import HostBlockManager
     peak, peak_kind = _peaks()
@@ -490,6 +501,37 @@ def run_op(args, local):
                     roofline={"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                               "frac": alg / (ms / 1e3) / 1e9 / peak, "alg_bytes_per_launch": alg,
                               "peak_kind": f"{peak_kind} hbm_gbs"})
+    elif args.op == "prefill":
+        wl = wcfg.prefill_config(dtype=args.prefill_dtype)
+        kp, vp, q = wcfg.prefill_inputs(wl, device=dev)
+        tables = torch.as_tensor(wl.tables(), device=dev)
+        lens = torch.full((wl.batch,), wl.length, dtype=torch.int32, device=dev)
+        qstart = torch.as_tensor(wl.qstart(), device=dev)
+        out = torch.empty_like(q)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2, rewritten before each launch
+        for _ in range(args.warmup):
+            api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b_ in ev:
+            flush.zero_()
+            a.record(stream)
+            api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b_) for a, b_ in ev) / K
+        flops = 4 * wl.D * wl.Hq * wl.causal_pairs()
+        tf = flops / (ms / 1e3) / 1e12
+        tpeak, tkind = _tensor_peak()
+        line.update(metric="pa_prefill TFLOP/s (causal pairs x 4 D x Hq)", value=tf, unit="TFLOP/s",
+                    ms_per_launch=ms, dtype=wl.dtype,
+                    config={"workload": wl.name, "batch": wl.batch, "history": wl.history, "chunk": wl.chunk,
+                            "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
+                            "l2": "flushed before every launch (256 MiB write)"},
+                    tokens_per_s=wl.batch * wl.chunk / (ms / 1e3),
+                    roofline={"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
+                              "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None},
+                    gpu_launches=K)
     else:
         res = {}
         for name, wl in (("longctx-f16-b8x32k", wcfg.config3(steps=K + args.warmup, layers=1)),
@@ -535,7 +577,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
     ap.add_argument("--kv", default="native", choices=["native", "fp8"], help="KV cache storage (fp8 = E4M3)")
-    ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host"],
+    ap.add_argument("--partition", type=int, default=0, help="decode partition tokens (0: the workload's)")
+    ap.add_argument("--prefill-dtype", default="bf16", choices=["f16", "bf16"], help="--op prefill storage dtype")
+    ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host", "prefill"],
                     help="step = the benchmark line; others measure one row of the path alone")
     args = ap.parse_args()
     D, G, b, dt = args.combo.split(",")

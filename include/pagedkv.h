@@ -209,6 +209,45 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
                         int partition_tokens, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_prefill -- paged prefill (chunked prefill) attention.  A chunk of new
+ * query tokens of each sequence attends causally to that sequence's paged
+ * history plus the chunk itself ("25. Paged attention and prefix caching",
+ * stretch exercise 4; "Chapter 7 Paged KV Cache and Memory Management", 4.1
+ * step 3: the key at position p is visible to the query at position i iff
+ * p <= i, the score scaled, masked keys weighted 0).
+ *
+ *   q, out        [total_q, Hq, D] `dtype` (f16 or bf16), device.  The rows of
+ *                 sequence s are qstart[s] .. qstart[s+1]-1 (its chunk, in
+ *                 position order).
+ *   qstart        int32 [batch + 1], device: cumulative query rows
+ *                 (qstart[0] = 0, qstart[batch] = total_q).
+ *   seq_lens      int32 [batch], device: each sequence's TOTAL length, the
+ *                 chunk included.  The chunk is the last C = qstart[s+1] -
+ *                 qstart[s] positions: chunk row r sits at position
+ *                 seq_lens[s] - C + r and sees positions 0 .. seq_lens[s] - C + r.
+ *                 The chunk's K/V rows must already be in the pools
+ *                 (pa_kv_append).
+ *   k_pool, v_pool, block_tables, max_blocks, num_blocks, block_size: as for
+ *                 pa_decode.
+ *   max_query_len the largest C of the batch (sizes the grid; a smaller
+ *                 value leaves the rows past it unwritten).
+ *   scale         multiplies q . k (typically 1/sqrt(D)).
+ *
+ * Output rows are rounded once from fp32 to `dtype`.  Tensor-core kernel
+ * only: D in {64, 128, 256}, Hq/Hkv in {1, 2, 4, 8}, b a multiple of 16 up to
+ * 256, num_blocks * Hkv * b < 2^31; other shapes, and f32, give
+ * PA_ERR_UNSUPPORTED.  No workspace.  On the device, a sequence whose
+ * length, chunk or qstart entries are inconsistent (C < 0, C > length,
+ * length above the table's capacity, rows outside [0, total_q]) is skipped
+ * and flagged PA_DEVERR_SEQLEN; a table entry outside the pool is skipped
+ * and flagged PA_DEVERR_TABLE.
+ */
+pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, const int32_t* qstart,
+                     int batch, int total_q, int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                     int block_size, float scale, pa_dtype dtype, void* stream);
+
+/*
  * pa_set_decode_kernel -- process-wide choice of the pa_decode partition
  * kernel (both compute the same result within the attention tolerance):
  *   PA_DECODE_AUTO  (default) tensor cores for fp16/bf16 pools, CUDA cores for fp32;

@@ -33,6 +33,8 @@ SIGNATURES = {
     "pa_kv_append_fp8": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     "pa_decode_fp8": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                              _f32, _i32, _vp, _sz, _vp]),
+    "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                          _f32, _i32, _vp]),
     "pa_set_decode_kernel": (_i32, [_i32]),
     "pa_selftest_wait_timeout": (_i32, [_i32, _vp]),
     "pa_get_device_error": (_i32, [C.POINTER(C.c_int), _vp]),

@@ -108,6 +108,30 @@ def pa_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale, partition_t
                         _stream(stream)), "pa_decode")
 
 
+def pa_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, qstart, scale, max_query_len=None,
+               stream=None) -> None:
+    """Causal attention of each sequence's chunk (rows qstart[s] .. qstart[s+1]-1 of
+    q [total_q, Hq, D]) over its paged history plus the chunk; seq_lens [B] are the
+    total lengths (chunk included), qstart [B+1] int32.  ``max_query_len`` is the
+    largest chunk (read from qstart, with a device sync, when None)."""
+    lib = load()
+    T, Hq, D = q.shape
+    N, Hkv, b, D2 = k_pool.shape
+    if D2 != D or tuple(out.shape) != tuple(q.shape) or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    B = seq_lens.shape[0]
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or qstart.shape != (B + 1,):
+        raise ValueError("block_tables must be [B, max_blocks], seq_lens [B] and qstart [B + 1]")
+    if max_query_len is None:
+        max_query_len = int((qstart[1:] - qstart[:-1]).max().item()) if B else 0
+    dt = k_pool.dtype
+    check(lib.pa_prefill(_dev(out, "out", dt), _dev(q, "q", dt), _dev(k_pool, "k_pool", dt),
+                         _dev(v_pool, "v_pool", dt), N, _dev(block_tables, "block_tables", torch.int32),
+                         block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32),
+                         _dev(qstart, "qstart", torch.int32), B, T, int(max_query_len), Hq, Hkv, D, b, float(scale),
+                         _dtype_id(k_pool), _stream(stream)), "pa_prefill")
+
+
 def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, partition_tokens=0,
                       stream=None) -> None:
     """pa_decode with the library's fixed scratch array instead of caller scratch

@@ -137,10 +137,11 @@ struct MmaCfg {
     static constexpr int BOX_BYTES = TILE * 128;       // 2 KiB, 1024-byte aligned in smem
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
-    // 2 stages x 4 warps (2 warps when a stage is >= 16 KiB; 4 stages for the
+    // 2 stages x 4 warps (2 warps when a stage is >= 16 KiB; 3 stages for the
     // 4 KiB stages of FP8 at D = 128): 32-64 KiB per CTA, so 3+ CTAs share an
     // SM; deeper rings measured slower on the long-context workload (fewer
-    // resident CTAs to cover each CTA's start and end).
+    // resident CTAs to cover each CTA's start and end, and to hide the
+    // latency of each warp's chain of dependent MMAs).
 #ifdef PA_MMA_WARPS
     static constexpr int NW = PA_MMA_WARPS;  // build-time override (tuning sweeps)
 #else
@@ -149,7 +150,7 @@ struct MmaCfg {
 #ifdef PA_MMA_STAGES
     static constexpr int STAGES = PA_MMA_STAGES;
 #else
-    static constexpr int STAGES = (F8 && STAGE_BYTES <= 4096) ? 4 : 2;
+    static constexpr int STAGES = (F8 && STAGE_BYTES <= 4096) ? 3 : 2;
 #endif
     static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_BYTES;
@@ -296,7 +297,8 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         unsigned char* vt = kt + C::TILE_BYTES;
         if (present) {
             // ---- scores S^T = K Q^T (16 tokens x 8 heads)
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            // two accumulators (even / odd k-steps) halve the chain of dependent MMAs
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
             const uint32_t kbase = smem_u32(kt);
             const int krow = lr + (lm & 1) * 8;
             if constexpr (F8) {
@@ -309,16 +311,18 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                     const uint32_t a1[4] = {e4m3x2_to_h2(r[2]), e4m3x2_to_h2(r[3]), e4m3x2_to_h2(r[2] >> 16),
                                             e4m3x2_to_h2(r[3] >> 16)};
                     mma16816<TM>(sc, a0, qb[ks][0], qb[ks][1]);
-                    mma16816<TM>(sc, a1, qb[ks + 1][0], qb[ks + 1][1]);
+                    mma16816<TM>(sc2, a1, qb[ks + 1][0], qb[ks + 1][1]);
                 }
             } else {
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     uint32_t a[4];
                     ldsm_x4(kbase + swz(krow, ks * 2 + (lm >> 1)), a);
-                    mma16816<TM>(sc, a, qb[ks][0], qb[ks][1]);
+                    mma16816<TM>((ks & 1) ? sc2 : sc, a, qb[ks][0], qb[ks][1]);
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
             // sc = {S[tok g][h0], S[tok g][h1], S[tok g+8][h0], S[tok g+8][h1]}
             const bool v0 = g < nv, v1 = g + 8 < nv;
             sc[0] = v0 ? sc[0] * sl2 : -INFINITY;

@@ -295,6 +295,50 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
     return from_cuda(q_dtype == PA_F16 ? pa::launch_decode_fp8_f16(p, st) : pa::launch_decode_fp8_bf16(p, st));
 }
 
+pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, const int32_t* qstart,
+                     int batch, int total_q, int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                     int block_size, float scale, pa_dtype dtype, void* stream) {
+    if (elt_size(dtype) == 0 || batch < 0 || batch > 65535 || total_q < 0 || max_query_len < 0 ||
+        num_q_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 || head_dim <= 0 || block_size <= 0 ||
+        max_blocks <= 0 || num_blocks <= 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+    if (dtype == PA_F32) return PA_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
+    if (static_cast<uint64_t>(num_blocks) * num_kv_heads * block_size >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_blocks) * block_size > (1LL << 30)) return PA_ERR_INVALID;
+    if (static_cast<int64_t>(total_q) * num_q_heads * head_dim >= (1LL << 40)) return PA_ERR_INVALID;
+    if (batch == 0 || total_q == 0 || max_query_len == 0) return PA_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !qstart) return PA_ERR_INVALID;
+    if (!al(out, 16) || !al(q, 16) || !al(k_pool, 16) || !al(v_pool, 16) || !al(block_tables, 4) ||
+        !al(seq_lens, 4) || !al(qstart, 4))
+        return PA_ERR_INVALID;
+    int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    pa::PrefillParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.qstart = qstart;
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks;
+    p.batch = batch;
+    p.total_q = total_q;
+    p.hq = num_q_heads;
+    p.hkv = num_kv_heads;
+    p.block_size = block_size;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return from_cuda(dtype == PA_F16 ? pa::launch_prefill_f16(p, k_pool, v_pool, head_dim, max_query_len, st)
+                                     : pa::launch_prefill_bf16(p, k_pool, v_pool, head_dim, max_query_len, st));
+}
+
 pa_status pa_selftest_wait_timeout(int limit_us, void* stream) {
     if (limit_us <= 0 || limit_us > 100000) return PA_ERR_INVALID;
     int* err = error_word();

@@ -41,6 +41,22 @@ struct DecodeParams {
     const float* v_scale;       // FP8 pools: [Hkv] scale of V codes (else null)
 };
 
+// Everything one pa_prefill call needs on the device.
+struct PrefillParams {
+    void* out;                    // [total_q, Hq, D] dtype
+    const void* q;                // [total_q, Hq, D] dtype
+    const int32_t* block_tables;  // [B, max_blocks]
+    const int32_t* seq_lens;      // [B] total length (history + chunk)
+    const int32_t* qstart;        // [B + 1] first query row of each sequence
+    int* err;
+    int64_t num_blocks;
+    int max_blocks;
+    int batch;
+    int total_q;
+    int hq, hkv, block_size;
+    float scale_log2;             // scale * log2(e)
+};
+
 // Launch `kernel` on `stream` allowing programmatic dependent launch (the
 // kernel itself waits for its predecessor with griddepcontrol.wait).
 template <typename... KArgs, typename... Args>
@@ -80,6 +96,11 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_fp8_f16(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_fp8_bf16(const DecodeParams& p, cudaStream_t stream);
 
+// Paged prefill (fp16 / bf16 pools, D in {64, 128, 256}, G in {1, 2, 4, 8}).
+cudaError_t launch_prefill_f16(const PrefillParams& p, const void* k_pool, const void* v_pool, int d, int max_q,
+                               cudaStream_t stream);
+cudaError_t launch_prefill_bf16(const PrefillParams& p, const void* k_pool, const void* v_pool, int d, int max_q,
+                                cudaStream_t stream);
 cudaError_t launch_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,
                                  const float* k_scale, const float* v_scale, const int64_t* slots,
                                  int64_t num_tokens, int64_t num_blocks, int hkv, int d, int block_size, int* err,

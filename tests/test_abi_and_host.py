@@ -65,6 +65,18 @@ def test_device_entry_points_validate_before_touching_cuda():
     # null tensors
     assert lib.pa_decode(null, null, null, null, 16, null, 4, null, 2, 4, 2, 64, 16, 0.1, 0, null, 0, 1,
                          null) == 1
+    # prefill: f32 and D = 96 unsupported; Hq not a multiple of Hkv; null tensors; empty batch is a no-op
+    #            out   q     kp    vp    N   tbl  mb  lens  qst   B  T  mq Hq Hkv D   b   scale dtype
+    assert lib.pa_prefill(null, null, null, null, 16, null, 4, null, null, 2, 8, 4, 4, 2, 64, 16, 0.1, 0,
+                          null) == 2
+    assert lib.pa_prefill(null, null, null, null, 16, null, 4, null, null, 2, 8, 4, 4, 2, 96, 16, 0.1, 1,
+                          null) == 2
+    assert lib.pa_prefill(null, null, null, null, 16, null, 4, null, null, 2, 8, 4, 5, 2, 64, 16, 0.1, 1,
+                          null) == 1
+    assert lib.pa_prefill(null, null, null, null, 16, null, 4, null, null, 2, 8, 4, 4, 2, 64, 16, 0.1, 1,
+                          null) == 1
+    assert lib.pa_prefill(null, null, null, null, 16, null, 4, null, null, 0, 0, 0, 4, 2, 64, 16, 0.1, 1,
+                          null) == 0
     ptrs = (C.c_void_p * 1)(None)
     assert lib.pa_copy_blocks(ptrs, ptrs, 1, null, 1, 16, 4096, null) == 1
     assert lib.pa_copy_blocks(ptrs, ptrs, 1, null, 1, 16, 4095, null) == 1

@@ -1,0 +1,175 @@
+"""Paged prefill on the GPU against the oracle (needs a GPU).
+
+Pools hold random values; slots past each sequence's length hold NaN, so any
+read of an unwritten slot shows.  The oracle computes each chunk row's causal
+attention from the stored values in fp64; the kernel must match within the
+tolerance of the storage dtype (f16 2e-3, bf16 1e-2, as for decode).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import blocks as oblocks
+from oracle import prefill as oprefill
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float16: 2e-3, torch.bfloat16: 1e-2}
+MANT = {torch.float16: 10, torch.bfloat16: 7}
+
+
+def _check(got, want, V, dtype, visible):
+    """Rows with >= 64 visible keys: the decode tolerance.  Every element: that
+    tolerance plus the rounding bound of a few-key average, 2^-(m+1) (|o| +
+    max|v|) -- P and the output are each rounded once to the dtype (m mantissa
+    bits), which a short row does not average away."""
+    err = np.abs(got - want)
+    vmax = float(np.nanmax(np.abs(V)))
+    bound = TOL[dtype] + 2.0 ** -(MANT[dtype] + 1) * (np.abs(want) + vmax)
+    assert (err <= bound).all(), float((err - bound).max())
+    long_rows = np.asarray(visible) >= 64
+    if long_rows.any():
+        assert err[long_rows].max() <= TOL[dtype]
+
+
+def _visible(lengths, chunks):
+    out = []
+    for L, C in zip(lengths, chunks):
+        out += [L - C + r + 1 for r in range(C)]
+    return out
+
+
+@pytest.fixture(scope="module")
+def api():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_66_gb300 import api as _api
+    return _api
+
+
+def _setup(lengths, chunks, Hq, Hkv, D, b, dtype, seed, extra=5):
+    gen = torch.Generator().manual_seed(seed)
+    need = sum(-(-L // b) for L in lengths)
+    N = need + extra
+    t = oblocks.SeqTables(N, b, torch.randperm(N, generator=gen).tolist())
+    for s, L in enumerate(lengths):
+        t.create(s)
+        t.reserve(s, L)
+        t.advance(s, L)
+    K = torch.randn((N, Hkv, b, D), generator=gen).to(dtype)
+    V = torch.randn((N, Hkv, b, D), generator=gen).to(dtype)
+    for s, L in enumerate(lengths):                       # unwritten tail slots: NaN
+        if L % b:
+            blk = t.tables[s][-1]
+            K[blk, :, L % b:] = float("nan")
+            V[blk, :, L % b:] = float("nan")
+    rows, lens = t.batch(range(len(lengths)))
+    qstart = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = torch.randn((int(qstart[-1]), Hq, D), generator=gen).to(dtype)
+    return K, V, q, torch.tensor(rows, dtype=torch.int32), torch.tensor(lens, dtype=torch.int32), \
+        torch.tensor(qstart, dtype=torch.int32)
+
+
+def _run(api, K, V, q, tables, lens, qstart, scale, max_q=None):
+    out = torch.full_like(q, float("nan")).cuda()
+    api.pa_prefill(out, q.cuda(), K.cuda(), V.cuda(), tables.cuda(), lens.cuda(), qstart.cuda(), scale,
+                   max_query_len=max_q)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+CASES = [
+    # (Hq, Hkv, D, b, lengths, chunks)
+    (32, 8, 128, 16, [100, 1, 64, 513], [100, 1, 20, 77]),
+    (8, 8, 64, 16, [37, 300], [37, 129]),
+    (16, 2, 256, 32, [70, 200], [70, 33]),
+    (8, 4, 128, 32, [1000], [300]),
+    (4, 1, 64, 16, [16, 17, 15], [16, 17, 15]),
+    (32, 4, 128, 16, [47, 8], [47, 8]),
+    (8, 1, 256, 16, [33], [2]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("case", CASES)
+def test_prefill_matches_oracle(api, dtype, case):
+    Hq, Hkv, D, b, lengths, chunks = case
+    K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype,
+                                           seed=hash((Hq, D, b, len(lengths))) & 0xFFFF)
+    scale = 1 / math.sqrt(D)
+    got = _run(api, K, V, q, tables, lens, qstart, scale)
+    assert api.pa_get_device_error() == 0
+    want = oprefill.paged_prefill_batch(q.double().numpy(), K.double().numpy(), V.double().numpy(),
+                                        tables.tolist(), lens.tolist(), qstart.tolist(), b, scale)
+    assert torch.isfinite(got).all()
+    _check(got.double().numpy(), want, V.double().numpy(), dtype, _visible(lengths, chunks))
+
+
+def test_prefill_chunk_of_one_equals_decode(api):
+    """A one-row chunk is decode at the sequence's last position."""
+    Hq, Hkv, D, b = 32, 8, 128, 16
+    lengths = [513, 40, 1]
+    K, V, q, tables, lens, qstart = _setup(lengths, [1, 1, 1], Hq, Hkv, D, b, torch.float16, seed=9)
+    got = _run(api, K, V, q, tables, lens, qstart, 0.088)
+    out = torch.empty_like(q).cuda()
+    n = api.pa_decode_workspace_size(3, Hq, D, tables.shape[1], b, 0)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
+    api.pa_decode(out, q.cuda(), K.cuda(), V.cuda(), tables.cuda(), lens.cuda(), 0.088, workspace=ws)
+    torch.cuda.synchronize()
+    assert (got - out.cpu()).abs().max().item() <= 2e-3
+
+
+def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api):
+    Hq, Hkv, D, b = 8, 2, 64, 16
+    K, V, q, tables, lens, qstart = _setup([20, 30], [5, 6], Hq, Hkv, D, b, torch.float16, seed=11)
+    lens[0] = 3                                           # chunk of 5 > length 3
+    got = _run(api, K, V, q, tables, lens, qstart, 0.125)
+    assert api.pa_get_device_error() == 4                 # PA_DEVERR_SEQLEN
+    assert torch.isnan(got[:5]).all()                     # skipped rows stay unwritten
+    want = oprefill.paged_prefill_batch(q[5:].double().numpy(), K.double().numpy(), V.double().numpy(),
+                                        tables[1:].tolist(), lens[1:].tolist(), [0, 6], b, 0.125)
+    assert np.abs(got[5:].double().numpy() - want).max() <= 2e-3
+
+
+def test_prefill_bad_table_entry_is_flagged(api):
+    Hq, Hkv, D, b = 8, 2, 64, 16
+    K, V, q, tables, lens, qstart = _setup([40], [40], Hq, Hkv, D, b, torch.float16, seed=12)
+    tables[0, 1] = K.shape[0] + 7
+    _run(api, K, V, q, tables, lens, qstart, 0.125)
+    assert api.pa_get_device_error() == 2                 # PA_DEVERR_TABLE
+
+
+def test_prefill_f32_unsupported(api):
+    K, V, q, tables, lens, qstart = _setup([20], [20], 4, 2, 64, 16, torch.float32, seed=13)
+    with pytest.raises(api.PagedKVError) as e:
+        _run(api, K, V, q, tables, lens, qstart, 0.125)
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_bench_workload_sampled_rows(api, dtype):
+    """The benchmark's launch (8 chunks of 1024 over 3072 cached tokens, Llama-3-8B
+    layer shape), inputs generated on the device as the benchmark does; sampled
+    rows checked one by one against the oracle."""
+    from oracle import attention as oatt
+    from workload import configs as wcfg
+    wl = wcfg.prefill_config(dtype=dtype)
+    kp, vp, q = wcfg.prefill_inputs(wl, device="cuda")
+    tables = torch.as_tensor(wl.tables(), device="cuda")
+    lens = torch.full((wl.batch,), wl.length, dtype=torch.int32, device="cuda")
+    qstart = torch.as_tensor(wl.qstart(), device="cuda")
+    out = torch.empty_like(q)
+    api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
+    torch.cuda.synchronize()
+    assert api.pa_get_device_error() == 0
+    K, V = kp.cpu(), vp.cpu()
+    got, qc = out.cpu().double().numpy(), q.cpu().double().numpy()
+    tol = TOL[wl.torch_dtype]
+    for s, r in [(0, 0), (0, 511), (3, 1023), (7, 64), (7, 1023)]:
+        pos = wl.history + r
+        Kh = oatt.gather_history(K, wl.tables()[s], pos + 1, wl.b)
+        Vh = oatt.gather_history(V, wl.tables()[s], pos + 1, wl.b)
+        want = oprefill.prefill_attention(qc[s * wl.chunk + r][None], Kh, Vh, wl.scale)[0]
+        assert np.abs(got[s * wl.chunk + r] - want).max() <= tol

@@ -239,3 +239,67 @@ def config5(D: int = 128, G: int = 4, b: int = 16, dtype: str = "bf16", steps: i
 
 def all_configs():
     return {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+
+
+# --------------------------------------------------------------------------- prefill
+
+@dataclass
+class PrefillWorkload:
+    """Chunked prefill of a Llama-3-8B-shaped layer: every sequence holds
+    ``history`` cached tokens and attends a ``chunk`` of new ones causally.
+    Blocks are scattered over the pool by a seeded permutation; K, V and q are
+    N(0, 1) rounded to the dtype (``prefill_inputs``)."""
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    b: int
+    dtype: str
+    batch: int
+    history: int
+    chunk: int
+    num_blocks: int
+    seed: int
+
+    @property
+    def length(self) -> int:
+        return self.history + self.chunk
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def tables(self) -> np.ndarray:
+        """int32 [batch, blocks per sequence] drawn from a seeded permutation of the pool."""
+        per = -(-self.length // self.b)
+        return _perm(self.seed, self.num_blocks)[:self.batch * per].reshape(self.batch, per)
+
+    def qstart(self) -> np.ndarray:
+        return (np.arange(self.batch + 1) * self.chunk).astype(np.int32)
+
+    def causal_pairs(self) -> int:
+        """(query row, visible key) pairs per query head: sum over the chunk of
+        history + r + 1."""
+        C, H = self.chunk, self.history
+        return self.batch * (C * H + C * (C + 1) // 2)
+
+
+def prefill_config(dtype: str = "bf16", batch: int = 8, history: int = 3072, chunk: int = 1024) -> PrefillWorkload:
+    per = -(-(history + chunk) // 16)
+    return PrefillWorkload(f"prefill-llama8b-{dtype}-b{batch}-h{history}-c{chunk}", Hq=32, Hkv=8, D=128, b=16,
+                           dtype=dtype, batch=batch, history=history, chunk=chunk,
+                           num_blocks=max(4096, batch * per + 64), seed=1006)
+
+
+def prefill_inputs(wl: PrefillWorkload, device="cpu"):
+    """Pools [N, Hkv, b, D] and packed q [batch * chunk, Hq, D] (seeded N(0, 1))."""
+    g = torch.Generator(device=device).manual_seed(wl.seed)
+    shape = (wl.num_blocks, wl.Hkv, wl.b, wl.D)
+    k = torch.randn(shape, generator=g, device=device).to(wl.torch_dtype)
+    v = torch.randn(shape, generator=g, device=device).to(wl.torch_dtype)
+    q = torch.randn((wl.batch * wl.chunk, wl.Hq, wl.D), generator=g, device=device).to(wl.torch_dtype)
+    return k, v, q
