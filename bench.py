@@ -502,6 +502,7 @@ def run_op(args, local):
                               "frac": alg / (ms / 1e3) / 1e9 / peak, "alg_bytes_per_launch": alg,
                               "peak_kind": f"{peak_kind} hbm_gbs"})
     elif args.op == "prefill":
+        api.pa_set_prefill_kernel(args.prefill_kernel)
         wl = wcfg.prefill_config(dtype=args.prefill_dtype)
         kp, vp, q = wcfg.prefill_inputs(wl, device=dev)
         tables = torch.as_tensor(wl.tables(), device=dev)
@@ -530,7 +531,8 @@ def run_op(args, local):
                             "l2": "flushed before every launch (256 MiB write)"},
                     tokens_per_s=wl.batch * wl.chunk / (ms / 1e3),
                     roofline={"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
-                              "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None},
+                              "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None,
+                              "kernel": f"pa_prefill ({args.prefill_kernel})"},
                     gpu_launches=K)
     else:
         res = {}
@@ -578,6 +580,7 @@ def main():
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
     ap.add_argument("--kv", default="native", choices=["native", "fp8"], help="KV cache storage (fp8 = E4M3)")
     ap.add_argument("--partition", type=int, default=0, help="decode partition tokens (0: the workload's)")
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc05"], help="--op prefill kernel")
     ap.add_argument("--prefill-dtype", default="bf16", choices=["f16", "bf16"], help="--op prefill storage dtype")
     ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host", "prefill"],
                     help="step = the benchmark line; others measure one row of the path alone")

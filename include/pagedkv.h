@@ -266,6 +266,24 @@ typedef enum pa_decode_kernel {
 pa_status pa_set_decode_kernel(pa_decode_kernel kernel);
 
 /*
+ * pa_set_prefill_kernel -- process-wide choice of the pa_prefill kernel (both
+ * compute the same result within the attention tolerance):
+ *   PA_PREFILL_AUTO  (default) PA_PREFILL_TC05 where it applies (D in
+ *                    {64, 128}), else PA_PREFILL_MMA;
+ *   PA_PREFILL_MMA   warp-level tensor-core kernel (mma m16n8k16), every D;
+ *   PA_PREFILL_TC05  tcgen05 kernel (accumulators in tensor memory) --
+ *                    pa_prefill then returns PA_ERR_UNSUPPORTED for D = 256.
+ * Returns PA_ERR_INVALID for any other value.
+ */
+typedef enum pa_prefill_kernel {
+    PA_PREFILL_AUTO = 0,
+    PA_PREFILL_MMA = 1,
+    PA_PREFILL_TC05 = 2
+} pa_prefill_kernel;
+
+pa_status pa_set_prefill_kernel(pa_prefill_kernel kernel);
+
+/*
  * pa_selftest_wait_timeout -- exercise the failure path of the bounded
  * device waits: launch one warp that waits on an mbarrier nothing completes,
  * giving up after `limit_us` microseconds (1..100000).  Afterwards

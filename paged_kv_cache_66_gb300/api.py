@@ -18,7 +18,7 @@ _TORCH_TO_ID = {torch.float32: DTYPE_IDS["f32"], torch.float16: DTYPE_IDS["f16"]
                 torch.bfloat16: DTYPE_IDS["bf16"]}
 
 __all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
-           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_get_device_error", "pa_status_string", "PagedKVError"]
+           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_set_prefill_kernel", "pa_get_device_error", "pa_status_string", "PagedKVError"]
 
 
 def _stream(stream):
@@ -201,6 +201,14 @@ DECODE_KERNELS = {"auto": 0, "simt": 1, "mma": 2}
 def pa_set_decode_kernel(kernel: str) -> None:
     """Process-wide choice of the decode kernel: "auto", "simt" or "mma"."""
     check(load().pa_set_decode_kernel(DECODE_KERNELS[kernel]), "pa_set_decode_kernel")
+
+
+PREFILL_KERNELS = {"auto": 0, "mma": 1, "tc05": 2}
+
+
+def pa_set_prefill_kernel(kernel: str) -> None:
+    """Process-wide pa_prefill kernel: "auto" (tcgen05 where it applies), "mma" or "tc05"."""
+    check(load().pa_set_prefill_kernel(PREFILL_KERNELS[kernel]), "pa_set_prefill_kernel")
 
 
 def pa_get_device_error(stream=None) -> int:

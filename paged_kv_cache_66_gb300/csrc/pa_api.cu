@@ -36,6 +36,7 @@ int* error_word() {
 }
 
 std::atomic<int> g_decode_kernel{PA_DECODE_AUTO};
+std::atomic<int> g_prefill_kernel{PA_PREFILL_AUTO};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -109,6 +110,12 @@ extern "C" {
 pa_status pa_set_decode_kernel(pa_decode_kernel kernel) {
     if (kernel != PA_DECODE_AUTO && kernel != PA_DECODE_SIMT && kernel != PA_DECODE_MMA) return PA_ERR_INVALID;
     g_decode_kernel.store(kernel);
+    return PA_OK;
+}
+
+pa_status pa_set_prefill_kernel(pa_prefill_kernel kernel) {
+    if (kernel != PA_PREFILL_AUTO && kernel != PA_PREFILL_MMA && kernel != PA_PREFILL_TC05) return PA_ERR_INVALID;
+    g_prefill_kernel.store(kernel);
     return PA_OK;
 }
 
@@ -334,6 +341,7 @@ pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v
     p.hkv = num_kv_heads;
     p.block_size = block_size;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.kernel = g_prefill_kernel.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return from_cuda(dtype == PA_F16 ? pa::launch_prefill_f16(p, k_pool, v_pool, head_dim, max_query_len, st)
                                      : pa::launch_prefill_bf16(p, k_pool, v_pool, head_dim, max_query_len, st));

@@ -1,0 +1,50 @@
+// Choice between the prefill kernels for one pa_prefill call: the tcgen05
+// kernel (prefill_tc05.cuh) for D in {64, 128} unless the caller forced the
+// warp-level one (prefill_mma.cuh), which covers every D.
+#pragma once
+
+#include "prefill_mma.cuh"
+#include "prefill_tc05.cuh"
+
+namespace pa {
+
+template <typename T, int D, int G>
+cudaError_t launch_prefill_path(const PrefillParams& p, const CUtensorMap& km, const CUtensorMap& vm, int max_q,
+                                cudaStream_t stream) {
+    if constexpr (D <= 128) {
+        if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05<T, D, G>(p, km, vm, max_q, stream);
+    } else {
+        if (p.kernel == PA_PREFILL_TC05) return cudaErrorNotSupported;
+    }
+    return launch_prefill<T, D, G>(p, km, vm, max_q, stream);
+}
+
+template <typename T, int D>
+cudaError_t dispatch_prefill_group(const PrefillParams& p, const CUtensorMap& km, const CUtensorMap& vm, int max_q,
+                                   cudaStream_t stream) {
+    switch (p.hq / p.hkv) {
+        case 1: return launch_prefill_path<T, D, 1>(p, km, vm, max_q, stream);
+        case 2: return launch_prefill_path<T, D, 2>(p, km, vm, max_q, stream);
+        case 4: return launch_prefill_path<T, D, 4>(p, km, vm, max_q, stream);
+        case 8: return launch_prefill_path<T, D, 8>(p, km, vm, max_q, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+template <typename T>
+cudaError_t dispatch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool, int d, int max_q,
+                             cudaStream_t stream) {
+    const uint64_t rows = static_cast<uint64_t>(p.num_blocks) * p.hkv * p.block_size;
+    if (rows >= (1ull << 31)) return cudaErrorNotSupported;
+    CUtensorMap km, vm;
+    if (!encode_pool_tmap(&km, k_pool, rows, d, 2) || !encode_pool_tmap(&vm, v_pool, rows, d, 2))
+        return cudaErrorInvalidValue;
+    switch (d) {
+        case 64: return dispatch_prefill_group<T, 64>(p, km, vm, max_q, stream);
+        case 128: return dispatch_prefill_group<T, 128>(p, km, vm, max_q, stream);
+        case 256: return dispatch_prefill_group<T, 256>(p, km, vm, max_q, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace pa

@@ -1,5 +1,5 @@
 // Paged prefill instantiations for f16 pools.
-#include "prefill_mma.cuh"
+#include "prefill_dispatch.cuh"
 
 namespace pa {
 

@@ -92,10 +92,23 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=["mma", "tc05"])
+def kernel(request, api):
+    api.pa_set_prefill_kernel(request.param)
+    yield request.param
+    api.pa_set_prefill_kernel("auto")
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("case", CASES)
-def test_prefill_matches_oracle(api, dtype, case):
+def test_prefill_matches_oracle(api, kernel, dtype, case):
     Hq, Hkv, D, b, lengths, chunks = case
+    if kernel == "tc05" and D == 256:
+        K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype, seed=1)
+        with pytest.raises(api.PagedKVError) as e:
+            _run(api, K, V, q, tables, lens, qstart, 0.1)
+        assert e.value.status == 2
+        return
     K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype,
                                            seed=hash((Hq, D, b, len(lengths))) & 0xFFFF)
     scale = 1 / math.sqrt(D)
@@ -107,7 +120,7 @@ def test_prefill_matches_oracle(api, dtype, case):
     _check(got.double().numpy(), want, V.double().numpy(), dtype, _visible(lengths, chunks))
 
 
-def test_prefill_chunk_of_one_equals_decode(api):
+def test_prefill_chunk_of_one_equals_decode(api, kernel):
     """A one-row chunk is decode at the sequence's last position."""
     Hq, Hkv, D, b = 32, 8, 128, 16
     lengths = [513, 40, 1]
@@ -121,7 +134,7 @@ def test_prefill_chunk_of_one_equals_decode(api):
     assert (got - out.cpu()).abs().max().item() <= 2e-3
 
 
-def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api):
+def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api, kernel):
     Hq, Hkv, D, b = 8, 2, 64, 16
     K, V, q, tables, lens, qstart = _setup([20, 30], [5, 6], Hq, Hkv, D, b, torch.float16, seed=11)
     lens[0] = 3                                           # chunk of 5 > length 3
@@ -133,7 +146,7 @@ def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api):
     assert np.abs(got[5:].double().numpy() - want).max() <= 2e-3
 
 
-def test_prefill_bad_table_entry_is_flagged(api):
+def test_prefill_bad_table_entry_is_flagged(api, kernel):
     Hq, Hkv, D, b = 8, 2, 64, 16
     K, V, q, tables, lens, qstart = _setup([40], [40], Hq, Hkv, D, b, torch.float16, seed=12)
     tables[0, 1] = K.shape[0] + 7
@@ -149,7 +162,7 @@ def test_prefill_f32_unsupported(api):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_prefill_bench_workload_sampled_rows(api, dtype):
+def test_prefill_bench_workload_sampled_rows(api, kernel, dtype):
     """The benchmark's launch (8 chunks of 1024 over 3072 cached tokens, Llama-3-8B
     layer shape), inputs generated on the device as the benchmark does; sampled
     rows checked one by one against the oracle."""
