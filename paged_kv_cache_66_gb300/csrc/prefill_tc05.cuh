@@ -8,24 +8,27 @@
 // Management", 4.1 step 3), same packing of rows: one CTA owns 128 query rows
 // -- (chunk token, query head of the group) pairs -- of one KV head.
 //
-// Per 64-key tile j of the history (a 3-stage TMA ring, each 16-key sub-tile
-// fetched through the block table):
-//   S_j = Q . K_j^T     tcgen05.mma M=128 N=64, A = Q (smem, K-major), B = K_j (smem, K-major)
-//                       into one of two TMEM S buffers, so the tensor core
-//                       computes S_{j+1} while the softmax threads read S_j;
-//   softmax             one thread per row: tcgen05.ld of its 64 scores,
-//                       causal mask, running max (base 2, lazy rescale of O
-//                       in TMEM only when the max grows by more than 2^8),
-//                       P_j = exp2(s - m) rounded to the dtype into shared
-//                       memory as a K-major operand;
-//   O += P_j . V_j      tcgen05.mma M=128 N=64 per 64 dims, A = P_j (smem),
-//                       B = V_j (smem, MN-major: keys are the K dimension).
-// Warps: 0-3 softmax (thread = row = TMEM lane), 4 producer (TMA), 5 MMA
-// issuer (one lane).  Hand-offs are mbarriers: TMA bytes (kv_full), MMA
-// completion through tcgen05.commit (s_full, o_ready, kv_empty), softmax
-// arrivals (p_full).  Barriers whose phases a waiter may skip come in pairs
-// by tile parity, so a parity wait never meets a barrier two phases ahead.
-// Every wait is bounded (1 s of %globaltimer, PA_DEVERR_TIMEOUT).
+// Per 64-key tile j of the history (a TMA ring of K/V stages, each 16-key
+// sub-tile fetched through the block table):
+//   S_j = Q . K_j^T     tcgen05.mma M=128 N=64, A = Q (tensor memory), B = K_j (smem,
+//                       K-major), into one of three TMEM S buffers;
+//   softmax             one thread per row: tcgen05.ld of its 64 scores, causal mask,
+//                       running max (base 2, lazy rescale of O only when the max grows by
+//                       more than 2^8), P_j = exp2(s - m) rounded to the dtype and stored
+//                       over the first half of S_j's columns;
+//   O_g += P_j . V_j    tcgen05.mma M=128 N=D, A = P_j (tensor memory), B = V_j (smem,
+//                       MN-major: keys are the K dimension).
+// Two softmax groups of four warps take alternate tiles (group g = j mod 2) into
+// their own accumulator O_g with their own running max and sum, so one group's
+// waits and loads overlap the other's exponentials; the two states are merged
+// at the end as partitions are (rescale each to the larger max, add, divide).
+// Warps: 0-7 softmax (warp w: group w / 4, rows 32 (w % 4) .. +31 = its TMEM
+// lanes), 8 producer (TMA), 9 MMA issuer (one lane, polling "K_j landed" and
+// "P_j written" so that neither waits behind the other).  Hand-offs are
+// mbarriers: TMA bytes (kv_full), MMA completion through tcgen05.commit
+// (s_full, o_ready per group, o_final, kv_empty), softmax arrivals (p_full).
+// Every wait is bounded (1 s of %globaltimer, PA_DEVERR_TIMEOUT), and no
+// barrier phase can run two ahead of a waiter's parity.
 //
 // Shared-memory operands use the 128-byte swizzle (the TMA layout): rows of
 // 128 bytes, 8-row atoms of 1024 bytes.  Descriptor: start >> 4, leading
@@ -70,6 +73,16 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
         : "memory");
 }
 
+// A operand in tensor memory: row m at lane m, two 16-bit values per column (low half = even k)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
 // arrives on `bar` once every tcgen05 operation this thread issued before has completed
 __device__ __forceinline__ void commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -101,8 +114,50 @@ __device__ __forceinline__ void st32(uint32_t addr, const uint32_t* r) {
         : "memory");
 }
 
+__device__ __forceinline__ void st16(uint32_t addr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(addr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// non-blocking test of a phase (try_wait may suspend the thread for a while when the phase is
+// not complete, which a loop polling two barriers cannot afford)
+__device__ __forceinline__ bool test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 2^x by the MUFU approximation (relative error ~2^-22; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// barrier `id` over `count` threads that also ANDs `pred` over them
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(out)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
 
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -112,23 +167,33 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 
 template <int D>
 struct Tc05Cfg {
-    static constexpr int BM = 128, BN = 64, STAGES = 3;
+    static constexpr int BM = 128, BN = 64;
+    static constexpr int NSB = 3;  // S buffers in tensor memory (P_j overwrites the first half of S_j)
+#ifdef PA_TC05_STAGES
+    static constexpr int STAGES = PA_TC05_STAGES;  // build-time override (tuning sweeps)
+#else
+    static constexpr int STAGES = D == 64 ? 8 : 5;
+#endif
     static constexpr int NBOX = D / 64;
-    static constexpr int Q_BYTES = NBOX * BM * 128;  // boxes of 128 rows x 128 B
     static constexpr int KV_BOX = BN * 128;          // 64 keys x 128 B
     static constexpr int K_BYTES = NBOX * KV_BOX;
     static constexpr int STAGE_BYTES = 2 * K_BYTES;  // K then V
-    static constexpr int P_BYTES = BM * BN * 2;      // 128 rows x 64 keys x 16 bit
-    static constexpr int KV_OFF = Q_BYTES;
-    static constexpr int P_OFF = KV_OFF + STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 1;  // kv_full, kv_empty, s_full, p_full, o_ready, q_full
+    static constexpr int KV_OFF = 0;
+    static constexpr int BAR_OFF = KV_OFF + STAGES * STAGE_BYTES;
+    // kv_full, kv_empty [STAGES]; s_full, p_full [NSB]; o_ready [2]; o_final; q_full
+    static constexpr int NBARS = 2 * STAGES + 2 * NSB + 2 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr size_t smem_bytes = 1024 + MISC_OFF + 16 + STAGES * 4;
-    static constexpr int O_COL = 2 * BN;
-    static constexpr uint32_t TMEM_COLS = 2 * BN + D <= 256 ? 256u : 512u;
-    static constexpr int THREADS = 192;
+    static constexpr int RED_OFF = MISC_OFF + 16 + 4 * STAGES;  // (m, l) of each group's rows [2][2][128]
+    static constexpr size_t smem_bytes = 1024 + RED_OFF + 4 * 128 * 4;
+    // tensor memory columns: O_0 [0, D), O_1 [D, 2D), Q [2D, 5D/2) (two 16-bit values per
+    // column), S buffers of 64
+    static constexpr int O_COL = 0, Q_COL = 2 * D, S_COL = 2 * D + D / 2;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int NSW = 8;  // softmax warps: two groups of four (one thread per row each)
+    static constexpr int PRODUCER = NSW, ISSUER = NSW + 1;
+    static constexpr int THREADS = (NSW + 2) * 32;
     static_assert(D == 64 || D == 128, "D in {64, 128}");
+    static_assert(S_COL + NSB * BN <= 512, "tensor memory columns");
 };
 
 template <typename T, int D, int G>
@@ -136,16 +201,17 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
     prefill_tc05(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap) {
     using C = Tc05Cfg<D>;
-    constexpr int STAGES = C::STAGES, NBOX = C::NBOX, BN = C::BN;
+    constexpr int STAGES = C::STAGES, NBOX = C::NBOX, BN = C::BN, NSB = C::NSB;
     constexpr int QT = C::BM / G;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* kv_empty = kv_full + STAGES;
     uint64_t* s_full = kv_empty + STAGES;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* o_ready = p_full + 2;
-    uint64_t* q_full = o_ready + 2;
+    uint64_t* p_full = s_full + NSB;
+    uint64_t* o_ready = p_full + NSB;
+    uint64_t* o_final = o_ready + 2;
+    uint64_t* q_full = o_final + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
     int* stage_ok = reinterpret_cast<int*>(smem + C::MISC_OFF + 16);  // loaded 16-key sub-tiles (bit mask)
 
@@ -173,15 +239,17 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             mbar_init(&kv_empty[i], 1);
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
-            mbar_init(&o_ready[i], 1);
         }
-        mbar_init(q_full, 128);
+        mbar_init(&o_ready[0], 1);
+        mbar_init(&o_ready[1], 1);
+        mbar_init(o_final, 1);
+        mbar_init(q_full, C::NSW * 32);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == C::ISSUER) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(C::TMEM_COLS)
                      : "memory");
@@ -193,7 +261,7 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_u32(smem);
 
-    if (warp == 4) {
+    if (warp == C::PRODUCER) {
         // ------------------------------------------------------------ producer
         const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
         const int n_sub = n_kv * 4;
@@ -212,128 +280,139 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             }
             for (int t0 = 0; t0 < 32 && u0 + t0 < n_sub; t0 += 4) {  // one 64-key tile per 4 lanes
                 const int j = (u0 + t0) / 4;
-                int r4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) r4[i] = __shfl_sync(0xffffffffu, row, t0 + i);
+                const int st = j % STAGES;
+                const int my_row = __shfl_sync(0xffffffffu, row, t0 + (lane & 3));
+                const unsigned mask = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFu;
                 if (lane == 0 && ok) {
-                    const int st = j % STAGES;
                     if (!mbar_wait_bounded(&kv_empty[st], ((j / STAGES) & 1) ^ 1)) {
                         flag_error(p.err, PA_DEVERR_TIMEOUT);
                         ok = false;
                     } else {
-                        int mask = 0, n = 0;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            if (r4[i] >= 0) {
-                                mask |= 1 << i;
-                                ++n;
-                            }
-                        stage_ok[st] = mask;
-                        mbar_arrive_expect_tx(&kv_full[st], static_cast<uint32_t>(n * 2 * NBOX * 2048));
-                        unsigned char* kd = smem + C::KV_OFF + st * C::STAGE_BYTES;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            if (r4[i] < 0) continue;
-#pragma unroll
-                            for (int bx = 0; bx < NBOX; ++bx) {
-                                tma_load_2d(kd + bx * C::KV_BOX + i * 2048, &kmap, bx * 64, r4[i], &kv_full[st]);
-                                tma_load_2d(kd + C::K_BYTES + bx * C::KV_BOX + i * 2048, &vmap, bx * 64, r4[i],
-                                            &kv_full[st]);
-                            }
-                        }
+                        stage_ok[st] = static_cast<int>(mask);
+                        // the stage's byte count is posted before any of its copies is issued
+                        mbar_arrive_expect_tx(&kv_full[st], static_cast<uint32_t>(__popc(mask) * 2 * NBOX * 2048));
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
+                // lanes 0-3 issue the copies of sub-tiles 0-3 side by side
+                if (ok && lane < 4 && my_row >= 0) {
+                    unsigned char* kd = smem + C::KV_OFF + st * C::STAGE_BYTES + lane * 2048;
+#pragma unroll
+                    for (int bx = 0; bx < NBOX; ++bx) {
+                        tma_load_2d(kd + bx * C::KV_BOX, &kmap, bx * 64, my_row, &kv_full[st]);
+                        tma_load_2d(kd + C::K_BYTES + bx * C::KV_BOX, &vmap, bx * 64, my_row, &kv_full[st]);
+                    }
+                }
+                __syncwarp();
             }
         }
         return;  // every copy issued is waited for by the MMA warp before the kernel ends
     }
 
-    if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+    if (warp == C::ISSUER) {
+        // ------------------------------------------------------------ MMA issuer (one lane)
+        // S_js = Q K_js^T into S buffer js % NSB once K_js has landed and that buffer's previous
+        // P has been consumed (js < jp + NSB); O += P_jp V_jp once the softmax has written P_jp.
+        // Both are polled so that neither waits behind the other.
         if (lane == 0) {
             constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
-            constexpr uint32_t ID_PV = tc05::idesc<T>(64, true);
+            constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
             bool ok = mbar_wait_bounded(q_full, 0);
             tc05::fence_after();
-            for (int j = 0; j <= n_kv && ok; ++j) {
-                if (j < n_kv) {
-                    const int st = j % STAGES;
-                    if (!mbar_wait_bounded(&kv_full[st], (j / STAGES) & 1)) {
-                        ok = false;
-                        break;
-                    }
+            int js = 0, jp = 0;
+            uint64_t t_last = global_timer_ns();
+            while (ok && jp < n_kv) {
+                bool progressed = false;
+                if (js < n_kv && js < jp + NSB && tc05::test_wait(&kv_full[js % STAGES], (js / STAGES) & 1)) {
                     tc05::fence_after();
-                    const uint32_t kb = sbase + C::KV_OFF + st * C::STAGE_BYTES;
+                    const uint32_t kb = sbase + C::KV_OFF + (js % STAGES) * C::STAGE_BYTES;
+                    const uint32_t sd = tmem + C::S_COL + (js % NSB) * BN;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t a = tc05::sdesc(sbase + (ks >> 2) * (C::BM * 128) + (ks & 3) * 32, 16, 1024);
                         const uint64_t b = tc05::sdesc(kb + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
-                        tc05::mma(tmem + (j & 1) * BN, a, b, ID_S, ks > 0);
+                        tc05::mma_ts(sd, tmem + C::Q_COL + ks * 8, b, ID_S, ks > 0);
                     }
-                    tc05::commit(&s_full[j & 1]);
+                    tc05::commit(&s_full[js % NSB]);
+                    ++js;
+                    progressed = true;
                 }
-                if (j >= 1) {
-                    const int jj = j - 1;
-                    if (!mbar_wait_bounded(&p_full[jj & 1], (jj >> 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
+                if (jp < js && tc05::test_wait(&p_full[jp % NSB], (jp / NSB) & 1)) {
                     tc05::fence_after();
-                    const int st = jj % STAGES;
+                    const int st = jp % STAGES;
                     const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
-                    const uint32_t pb = sbase + C::P_OFF + (jj & 1) * C::P_BYTES;
+                    const uint32_t pa = tmem + C::S_COL + (jp % NSB) * BN;  // P_jp: key k at column k / 2
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t a = tc05::sdesc(pb + kk * 32, 16, 1024);
-#pragma unroll
-                        for (int bx = 0; bx < NBOX; ++bx) {
-                            const uint64_t b = tc05::sdesc(vb + bx * C::KV_BOX + kk * 2048, C::KV_BOX, 1024);
-                            tc05::mma(tmem + C::O_COL + bx * 64, a, b, ID_PV, (jj > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        // N = D in one MMA: the 64-dim boxes of V are KV_BOX apart (leading byte offset)
+                        const uint64_t b = tc05::sdesc(vb + kk * 2048, C::KV_BOX, 1024);
+                        tc05::mma_ts(tmem + C::O_COL + (jp & 1) * D, pa + kk * 8, b, ID_PV,
+                                     (jp > 1 || kk > 0) ? 1u : 0u);
                     }
-                    tc05::commit(&o_ready[jj & 1]);
+                    tc05::commit(&o_ready[jp & 1]);
                     tc05::commit(&kv_empty[st]);
+                    ++jp;
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = global_timer_ns();
+                } else if (global_timer_ns() - t_last > 1000000000ull) {
+                    ok = false;
                 }
             }
-            if (!ok) flag_error(p.err, PA_DEVERR_TIMEOUT);
+            if (ok) tc05::commit(o_final);
+            else flag_error(p.err, PA_DEVERR_TIMEOUT);
         }
         __syncwarp();
-        tc05::named_sync(1, 160);
+        tc05::named_sync(1, (C::NSW + 1) * 32);
         tc05::fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
                      : "memory");
         return;
     }
 
-    // ------------------------------------------------------------ softmax warps (thread = row)
-    const int r = tid;
+    // ------------------------------------------------------------ softmax warps
+    const int r = tid & 127, g = tid >> 7;  // row, group
+    const int wq = warp & 3;
     const int tok = tok0 + r / G;
     const bool valid = tok < Cq;
     const int pos = valid ? base + tok : -1;
     const int head = kvh * G + r % G;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // position of the first row of this warp's 32 (every valid row of the warp is at or after it)
+    const int warp_tok = tok0 + (wq * 32) / G;
+    const int warp_pos_min = warp_tok < Cq ? base + warp_tok : -1;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t o_addr = lane_addr + C::O_COL + g * D;
+    float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+    constexpr int DH = D / 2;
     {
-        // this row of Q into the K-major swizzled operand (zeros for rows past the chunk)
-        const uint4* qrow =
-            reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D);
+        // half g of Q row r into tensor memory (dims 2c, 2c + 1 in column c; zeros past the chunk)
+        const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                           (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + g * DH);
+        uint32_t w[DH / 2];
 #pragma unroll
-        for (int bx = 0; bx < NBOX; ++bx)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = valid ? __ldg(qrow + bx * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(smem + bx * (C::BM * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v;
-            }
-        fence_proxy_async_smem();
+        for (int i = 0; i < DH / 8; ++i) {
+            const uint4 v = valid ? __ldg(qrow + i) : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        if constexpr (DH / 2 == 32) {
+            tc05::st32(lane_addr + C::Q_COL + g * (DH / 2), w);
+        } else {
+            tc05::st16(lane_addr + C::Q_COL + g * (DH / 2), w);
+        }
+        tc05::wait_st();
+        tc05::fence_before();
         mbar_arrive(q_full);
     }
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-        const int st = j % STAGES;
-        // every decision that guards a tcgen05.ld / st is warp-uniform (those are .sync.aligned)
-        bool got = mbar_wait_bounded(&kv_full[st], (j / STAGES) & 1) && mbar_wait_bounded(&s_full[j & 1], (j >> 1) & 1);
+    for (int j = g; j < n_kv; j += 2) {
+        const int st = j % STAGES, sb = j % NSB;
+        // decisions that guard a tcgen05.ld / st are warp-uniform (those are .sync.aligned)
+        const bool got = mbar_wait_bounded(&kv_full[st], (j / STAGES) & 1) && mbar_wait_bounded(&s_full[sb], (j / NSB) & 1);
         if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
@@ -341,26 +420,45 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
         tc05::fence_after();
         const int key0 = j * BN;
         const int okmask = stage_ok[st];
+        const uint32_t sa = lane_addr + C::S_COL + sb * BN;
         uint32_t sr[64];
-        tc05::ld32(lane_addr + (j & 1) * BN, sr);
-        tc05::ld32(lane_addr + (j & 1) * BN + 32, sr + 32);
+        tc05::ld32(sa, sr);
+        tc05::ld32(sa + 32, sr + 32);
         tc05::wait_ld();
-        float sv[64];
-        float mx = -INFINITY;
+        // interior tile: every valid row of the warp sees all 64 keys and the scale is positive,
+        // so the row max is the raw max times the scale
+        const bool interior = okmask == 0xF && key0 + BN - 1 <= warp_pos_min && sl2 > 0.f;
+        // masked tiles keep their scores pre-scaled (masked: -inf) in sr; interior ones raw
+        float mx;
+        {
+            float t[8];
+            if (interior) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const bool vis = key0 + c <= pos && ((okmask >> (c >> 4)) & 1);
-            sv[c] = vis ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
+                for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(sr[i]);
+#pragma unroll
+                for (int c = 8; c < 64; ++c) t[c & 7] = fmaxf(t[c & 7], __uint_as_float(sr[c]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const bool vis = key0 + c <= pos && ((okmask >> (c >> 4)) & 1);
+                    const float x = vis ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+                    sr[c] = __float_as_uint(x);
+                    t[c & 7] = fmaxf(t[c & 7], x);
+                }
+            }
+            mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
+            if (interior) mx *= sl2;
         }
-        // lazy rescale per row; O (in TMEM) is rescaled for the whole warp when any row needs it,
-        // once P_{j-1} . V_{j-1} has landed, each lane by its own factor (1 when it keeps its max)
+        // lazy rescale per row; this group's O (in TMEM) is rescaled for the whole warp when any
+        // row needs it, once the group's previous P . V (tile j - 2) has landed, each lane by its
+        // own factor
         const bool grow = mx > m + kLazyRescale;
         const bool scale_o = grow && m != -INFINITY;
-        const float a = scale_o ? exp2f(m - mx) : 1.f;
-        if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
-            got = mbar_wait_bounded(&o_ready[(j - 1) & 1], ((j - 1) >> 1) & 1);
-            if (!__all_sync(0xffffffffu, got)) {
+        const float a = scale_o ? tc05::fast_exp2(m - mx) : 1.f;
+        if (j >= 2 && __any_sync(0xffffffffu, scale_o)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[g], ((j - 2) >> 1) & 1))) {
                 ok = false;
                 break;
             }
@@ -368,31 +466,36 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
-                tc05::ld32(lane_addr + C::O_COL + c0, o);
+                tc05::ld32(o_addr + c0, o);
                 tc05::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                tc05::st32(lane_addr + C::O_COL + c0, o);
+                tc05::st32(o_addr + c0, o);
             }
-            tc05::wait_st();
         }
         if (grow) {
             l *= a;
             m = mx;
         }
         const float ms = m == -INFINITY ? 0.f : m;
-        unsigned char* prow = smem + C::P_OFF + (j & 1) * C::P_BYTES + r * 128;
+        // P_j = 2^(v * mul - m) in one FFMA and one ex2 (interior: v raw, mul = scale; masked: v
+        // pre-scaled, mul = 1); key c at column c / 2 of S buffer sb, over this lane's own scores
+        const float mul = interior ? sl2 : 1.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t w[4];
+        for (int hq = 0; hq < 2; ++hq) {
+            uint32_t pw[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float e0 = exp2f(sv[c * 8 + 2 * i] - ms), e1 = exp2f(sv[c * 8 + 2 * i + 1] - ms);
-                l += e0 + e1;
-                w[i] = pack2<T>(e0, e1);
+            for (int i = 0; i < 16; ++i) {
+                const int c = hq * 32 + 2 * i;
+                const float e0 = tc05::fast_exp2(fmaf(__uint_as_float(sr[c]), mul, -ms));
+                const float e1 = tc05::fast_exp2(fmaf(__uint_as_float(sr[c + 1]), mul, -ms));
+                ls[i & 3] += e0 + e1;
+                pw[i] = pack2<T>(e0, e1);
             }
-            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            tc05::st16(sa + hq * 16, pw);
         }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero them
         if (key0 + BN > L || okmask != 0xF) {
             unsigned char* vt = smem + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
@@ -402,39 +505,56 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
                     *reinterpret_cast<uint4*>(vt + (rest >> 3) * C::KV_BOX + key * 128 + (rest & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
             }
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        tc05::wait_st();
         tc05::fence_before();
-        mbar_arrive(&p_full[j & 1]);
+        mbar_arrive(&p_full[sb]);
     }
     griddep_launch_dependents();
-    if (ok) ok = mbar_wait_bounded(&o_ready[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1);
-    if (__all_sync(0xffffffffu, ok)) {
+    // merge the groups' states of row r: each O_g scaled by 2^(m_g - M), the normalisers alike;
+    // group g writes dims [g D/2, (g + 1) D/2)
+    red[g * 256 + r] = m;
+    red[g * 256 + 128 + r] = l;
+    const bool all_ok = tc05::bar_and(2, C::NSW * 32, ok);
+    const float m0 = red[r], l0 = red[128 + r], m1 = red[256 + r], l1 = red[384 + r];
+    const float M = fmaxf(m0, m1);
+    const float f0 = m0 == -INFINITY ? 0.f : tc05::fast_exp2(m0 - M);
+    const float f1 = m1 == -INFINITY ? 0.f : tc05::fast_exp2(m1 - M);
+    const float den = f0 * l0 + f1 * l1;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const bool done = all_ok && mbar_wait_bounded(o_final, 0);
+    if (__all_sync(0xffffffffu, done)) {
         tc05::fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D;
+        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + g * DH;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tc05::ld32(lane_addr + C::O_COL + c0, o);
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+            uint32_t x0[32], x1[32];
+            tc05::ld32(lane_addr + C::O_COL + g * DH + c0, x0);
+            tc05::ld32(lane_addr + C::O_COL + D + g * DH + c0, x1);
             tc05::wait_ld();
             if (valid) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)  // a group that saw no tile never wrote its O: select it out
+                    v[i] = ((f0 != 0.f ? f0 * __uint_as_float(x0[i]) : 0.f) +
+                            (f1 != 0.f ? f1 * __uint_as_float(x1[i]) : 0.f)) * inv;
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
-                    uint4 v;
-                    v.x = pack2<T>(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
-                    v.y = pack2<T>(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-                    v.z = pack2<T>(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
-                    v.w = pack2<T>(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
-                    *reinterpret_cast<uint4*>(orow + c0 + i) = v;
+                    uint4 u;
+                    u.x = pack2<T>(v[i], v[i + 1]);
+                    u.y = pack2<T>(v[i + 2], v[i + 3]);
+                    u.z = pack2<T>(v[i + 4], v[i + 5]);
+                    u.w = pack2<T>(v[i + 6], v[i + 7]);
+                    *reinterpret_cast<uint4*>(orow + c0 + i) = u;
                 }
             }
         }
-    } else {
-        if (threadIdx.x % 32 == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
+    } else if (lane == 0) {
+        flag_error(p.err, PA_DEVERR_TIMEOUT);
     }
     tc05::fence_before();
-    tc05::named_sync(1, 160);
+    tc05::named_sync(1, (C::NSW + 1) * 32);
 }
 
 template <typename T, int D, int G>
