@@ -8,26 +8,25 @@
 // Management", 4.1 step 3), same packing of rows: one CTA owns 128 query rows
 // -- (chunk token, query head of the group) pairs -- of one KV head.
 //
-// Per 64-key tile j of the history (a TMA ring of K/V stages, each 16-key
-// sub-tile fetched through the block table):
-//   S_j = Q . K_j^T     tcgen05.mma M=128 N=64, A = Q (tensor memory), B = K_j (smem,
-//                       K-major), into one of three TMEM S buffers;
-//   softmax             one thread per row: tcgen05.ld of its 64 scores, causal mask,
-//                       running max (base 2, lazy rescale of O only when the max grows by
-//                       more than 2^8), P_j = exp2(s - m) rounded to the dtype and stored
-//                       over the first half of S_j's columns;
-//   O_g += P_j . V_j    tcgen05.mma M=128 N=D, A = P_j (tensor memory), B = V_j (smem,
-//                       MN-major: keys are the K dimension).
-// Two softmax groups of four warps take alternate tiles (group g = j mod 2) into
-// their own accumulator O_g with their own running max and sum, so one group's
-// waits and loads overlap the other's exponentials; the two states are merged
-// at the end as partitions are (rescale each to the larger max, add, divide).
-// Warps: 0-7 softmax (warp w: group w / 4, rows 32 (w % 4) .. +31 = its TMEM
-// lanes), 8 producer (TMA), 9 MMA issuer (one lane, polling "K_j landed" and
-// "P_j written" so that neither waits behind the other).  Hand-offs are
-// mbarriers: TMA bytes (kv_full), MMA completion through tcgen05.commit
-// (s_full, o_ready per group, o_final, kv_empty), softmax arrivals (p_full).
-// Every wait is bounded (1 s of %globaltimer, PA_DEVERR_TIMEOUT), and no
+// One CTA owns 256 query rows of one KV head as two 128-row tiles X = A, B that
+// share every K/V tile staged in shared memory (twice the FLOPs per copied byte
+// of a single tile).  Per 64-key tile j of the history (a TMA ring of K/V
+// stages, each 16-key sub-tile fetched through the block table), for each X:
+//   S_Xj = Q_X . K_j^T   tcgen05.mma M=128 N=64, A = Q_X (smem, K-major), B = K_j (smem,
+//                        K-major), into one of two TMEM S buffers of tile X;
+//   softmax              one thread per row (group X = warps 4X .. 4X+3): tcgen05.ld of its
+//                        64 scores, causal mask, running max (base 2, lazy rescale of O_X
+//                        only when the max grows by more than 2^8), P_Xj = exp2(s - m)
+//                        rounded to the dtype and stored over the first half of S_Xj;
+//   O_X += P_Xj . V_j    tcgen05.mma M=128 N=D, A = P_Xj (tensor memory), B = V_j (smem,
+//                        MN-major: keys are the K dimension).
+// Warps: 0-7 softmax (warp w: tile w / 4, rows 32 (w % 4) .. +31 = its TMEM lanes),
+// 8 producer (TMA, four lanes issuing), 9 MMA issuer (one lane, polling the four
+// streams S_A, S_B, P_A, P_B with mbarrier.test_wait and issuing whichever is ready;
+// a K/V stage is released once both tiles' P . V on it have been issued).
+// Hand-offs are mbarriers: TMA bytes (kv_full), MMA completion through
+// tcgen05.commit (s_full, o_ready per tile, o_final, kv_empty), softmax arrivals
+// (p_full).  Every wait is bounded (1 s of %globaltimer, PA_DEVERR_TIMEOUT), and no
 // barrier phase can run two ahead of a waiter's parity.
 //
 // Shared-memory operands use the 128-byte swizzle (the TMA layout): rows of
@@ -167,33 +166,33 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 
 template <int D>
 struct Tc05Cfg {
-    static constexpr int BM = 128, BN = 64;
-    static constexpr int NSB = 3;  // S buffers in tensor memory (P_j overwrites the first half of S_j)
+    static constexpr int BM = 256, BN = 64;  // two 128-row query tiles; 64 keys per K/V tile
+    static constexpr int NSB = 2;            // S buffers per query tile (P_j overwrites the first half of S_j)
 #ifdef PA_TC05_STAGES
     static constexpr int STAGES = PA_TC05_STAGES;  // build-time override (tuning sweeps)
 #else
-    static constexpr int STAGES = D == 64 ? 8 : 5;
+    static constexpr int STAGES = D == 64 ? 8 : 4;
 #endif
     static constexpr int NBOX = D / 64;
+    static constexpr int QBOX = 128 * 128;           // 128 rows x 128 B
+    static constexpr int Q_BYTES = 2 * NBOX * QBOX;  // both tiles
     static constexpr int KV_BOX = BN * 128;          // 64 keys x 128 B
     static constexpr int K_BYTES = NBOX * KV_BOX;
     static constexpr int STAGE_BYTES = 2 * K_BYTES;  // K then V
-    static constexpr int KV_OFF = 0;
+    static constexpr int KV_OFF = Q_BYTES;
     static constexpr int BAR_OFF = KV_OFF + STAGES * STAGE_BYTES;
-    // kv_full, kv_empty [STAGES]; s_full, p_full [NSB]; o_ready [2]; o_final; q_full
-    static constexpr int NBARS = 2 * STAGES + 2 * NSB + 2 + 2;
+    // kv_full, kv_empty [STAGES]; s_full, p_full [2 tiles x NSB]; o_ready [2]; o_final; q_full
+    static constexpr int NBARS = 2 * STAGES + 4 * NSB + 2 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int RED_OFF = MISC_OFF + 16 + 4 * STAGES;  // (m, l) of each group's rows [2][2][128]
-    static constexpr size_t smem_bytes = 1024 + RED_OFF + 4 * 128 * 4;
-    // tensor memory columns: O_0 [0, D), O_1 [D, 2D), Q [2D, 5D/2) (two 16-bit values per
-    // column), S buffers of 64
-    static constexpr int O_COL = 0, Q_COL = 2 * D, S_COL = 2 * D + D / 2;
+    static constexpr size_t smem_bytes = 1024 + MISC_OFF + 16 + 4 * STAGES;
+    // tensor memory columns: O_A [0, D), O_B [D, 2D), S buffers of tile X at 2D + (X NSB + b) 64
+    static constexpr int O_COL = 0, S_COL = 2 * D;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NSW = 8;  // softmax warps: two groups of four (one thread per row each)
+    static constexpr int NSW = 8;  // softmax warps: two groups of four, one thread per row
     static constexpr int PRODUCER = NSW, ISSUER = NSW + 1;
     static constexpr int THREADS = (NSW + 2) * 32;
     static_assert(D == 64 || D == 128, "D in {64, 128}");
-    static_assert(S_COL + NSB * BN <= 512, "tensor memory columns");
+    static_assert(S_COL + 2 * NSB * BN <= 512, "tensor memory columns");
 };
 
 template <typename T, int D, int G>
@@ -207,9 +206,9 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* kv_empty = kv_full + STAGES;
-    uint64_t* s_full = kv_empty + STAGES;
-    uint64_t* p_full = s_full + NSB;
-    uint64_t* o_ready = p_full + NSB;
+    uint64_t* s_full = kv_empty + STAGES;  // [X * NSB + b]
+    uint64_t* p_full = s_full + 2 * NSB;
+    uint64_t* o_ready = p_full + 2 * NSB;  // [X]
     uint64_t* o_final = o_ready + 2;
     uint64_t* q_full = o_final + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
@@ -239,7 +238,7 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             mbar_init(&kv_empty[i], 1);
         }
 #pragma unroll
-        for (int i = 0; i < NSB; ++i) {
+        for (int i = 0; i < 2 * NSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
         }
@@ -311,47 +310,54 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
 
     if (warp == C::ISSUER) {
         // ------------------------------------------------------------ MMA issuer (one lane)
-        // S_js = Q K_js^T into S buffer js % NSB once K_js has landed and that buffer's previous
-        // P has been consumed (js < jp + NSB); O += P_jp V_jp once the softmax has written P_jp.
-        // Both are polled so that neither waits behind the other.
+        // S_Xj once K_j has landed and tile X's S buffer j % NSB has been consumed (j < jp_X + NSB);
+        // O_X += P_Xj V_j once the softmax of tile X has written P_Xj.  The four streams are
+        // polled so that none waits behind another.
         if (lane == 0) {
             constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
             constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
             bool ok = mbar_wait_bounded(q_full, 0);
             tc05::fence_after();
-            int js = 0, jp = 0;
+            int js[2] = {0, 0}, jp[2] = {0, 0};
             uint64_t t_last = global_timer_ns();
-            while (ok && jp < n_kv) {
+            while (ok && (jp[0] < n_kv || jp[1] < n_kv)) {
                 bool progressed = false;
-                if (js < n_kv && js < jp + NSB && tc05::test_wait(&kv_full[js % STAGES], (js / STAGES) & 1)) {
-                    tc05::fence_after();
-                    const uint32_t kb = sbase + C::KV_OFF + (js % STAGES) * C::STAGE_BYTES;
-                    const uint32_t sd = tmem + C::S_COL + (js % NSB) * BN;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t b = tc05::sdesc(kb + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
-                        tc05::mma_ts(sd, tmem + C::Q_COL + ks * 8, b, ID_S, ks > 0);
-                    }
-                    tc05::commit(&s_full[js % NSB]);
-                    ++js;
-                    progressed = true;
-                }
-                if (jp < js && tc05::test_wait(&p_full[jp % NSB], (jp / NSB) & 1)) {
-                    tc05::fence_after();
-                    const int st = jp % STAGES;
-                    const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
-                    const uint32_t pa = tmem + C::S_COL + (jp % NSB) * BN;  // P_jp: key k at column k / 2
+                for (int X = 0; X < 2; ++X) {
+                    const int j = js[X];
+                    if (j < n_kv && j < jp[X] + NSB && tc05::test_wait(&kv_full[j % STAGES], (j / STAGES) & 1)) {
+                        tc05::fence_after();
+                        const uint32_t kb = sbase + C::KV_OFF + (j % STAGES) * C::STAGE_BYTES;
+                        const uint32_t qa = sbase + X * NBOX * C::QBOX;
+                        const uint32_t sd = tmem + C::S_COL + (X * NSB + j % NSB) * BN;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        // N = D in one MMA: the 64-dim boxes of V are KV_BOX apart (leading byte offset)
-                        const uint64_t b = tc05::sdesc(vb + kk * 2048, C::KV_BOX, 1024);
-                        tc05::mma_ts(tmem + C::O_COL + (jp & 1) * D, pa + kk * 8, b, ID_PV,
-                                     (jp > 1 || kk > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint64_t a = tc05::sdesc(qa + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
+                            const uint64_t b = tc05::sdesc(kb + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
+                            tc05::mma(sd, a, b, ID_S, ks > 0);
+                        }
+                        tc05::commit(&s_full[X * NSB + j % NSB]);
+                        ++js[X];
+                        progressed = true;
                     }
-                    tc05::commit(&o_ready[jp & 1]);
-                    tc05::commit(&kv_empty[st]);
-                    ++jp;
-                    progressed = true;
+                    const int t = jp[X];
+                    if (t < js[X] && tc05::test_wait(&p_full[X * NSB + t % NSB], (t / NSB) & 1)) {
+                        tc05::fence_after();
+                        const int st = t % STAGES;
+                        const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
+                        const uint32_t pa = tmem + C::S_COL + (X * NSB + t % NSB) * BN;  // key k at column k / 2
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // N = D in one MMA: the 64-dim boxes of V are KV_BOX apart (leading byte offset)
+                            const uint64_t b = tc05::sdesc(vb + kk * 2048, C::KV_BOX, 1024);
+                            tc05::mma_ts(tmem + C::O_COL + X * D, pa + kk * 8, b, ID_PV, (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc05::commit(&o_ready[X]);
+                        // the stage is free once both tiles' P . V on it have completed
+                        if (jp[1 - X] > t) tc05::commit(&kv_empty[st]);
+                        ++jp[X];
+                        progressed = true;
+                    }
                 }
                 if (progressed) {
                     t_last = global_timer_ns();
@@ -370,47 +376,38 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
         return;
     }
 
-    // ------------------------------------------------------------ softmax warps
-    const int r = tid & 127, g = tid >> 7;  // row, group
+    // ------------------------------------------------------------ softmax warps (thread = row)
+    const int X = warp >> 2, r = tid & 127;  // query tile, row within it
     const int wq = warp & 3;
-    const int tok = tok0 + r / G;
+    const int prow_id = X * 128 + r;  // packed row of the CTA
+    const int tok = tok0 + prow_id / G;
     const bool valid = tok < Cq;
     const int pos = valid ? base + tok : -1;
-    const int head = kvh * G + r % G;
+    const int head = kvh * G + prow_id % G;
     // position of the first row of this warp's 32 (every valid row of the warp is at or after it)
-    const int warp_tok = tok0 + (wq * 32) / G;
+    const int warp_tok = tok0 + (X * 128 + wq * 32) / G;
     const int warp_pos_min = warp_tok < Cq ? base + warp_tok : -1;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t o_addr = lane_addr + C::O_COL + g * D;
-    float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
-    constexpr int DH = D / 2;
+    const uint32_t o_addr = lane_addr + C::O_COL + X * D;
     {
-        // half g of Q row r into tensor memory (dims 2c, 2c + 1 in column c; zeros past the chunk)
-        const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                           (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + g * DH);
-        uint32_t w[DH / 2];
+        // Q row into tile X's K-major swizzled operand (zeros past the chunk)
+        const uint4* qrow =
+            reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D);
+        unsigned char* qx = smem + X * NBOX * C::QBOX;
 #pragma unroll
-        for (int i = 0; i < DH / 8; ++i) {
-            const uint4 v = valid ? __ldg(qrow + i) : make_uint4(0u, 0u, 0u, 0u);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
+        for (int cc = 0; cc < D / 8; ++cc) {
+            const int bx = cc >> 3, c = cc & 7;
+            const uint4 v = valid ? __ldg(qrow + cc) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(qx + bx * C::QBOX + r * 128 + ((c ^ (r & 7)) << 4)) = v;
         }
-        if constexpr (DH / 2 == 32) {
-            tc05::st32(lane_addr + C::Q_COL + g * (DH / 2), w);
-        } else {
-            tc05::st16(lane_addr + C::Q_COL + g * (DH / 2), w);
-        }
-        tc05::wait_st();
-        tc05::fence_before();
+        fence_proxy_async_smem();
         mbar_arrive(q_full);
     }
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = g; j < n_kv; j += 2) {
-        const int st = j % STAGES, sb = j % NSB;
+    for (int j = 0; j < n_kv; ++j) {
+        const int st = j % STAGES, sb = X * NSB + j % NSB;
         // decisions that guard a tcgen05.ld / st are warp-uniform (those are .sync.aligned)
         const bool got = mbar_wait_bounded(&kv_full[st], (j / STAGES) & 1) && mbar_wait_bounded(&s_full[sb], (j / NSB) & 1);
         if (!__all_sync(0xffffffffu, got)) {
@@ -426,9 +423,9 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
         tc05::ld32(sa + 32, sr + 32);
         tc05::wait_ld();
         // interior tile: every valid row of the warp sees all 64 keys and the scale is positive,
-        // so the row max is the raw max times the scale
+        // so the row max is the raw max times the scale; masked tiles keep their scores
+        // pre-scaled (masked: -inf) in sr
         const bool interior = okmask == 0xF && key0 + BN - 1 <= warp_pos_min && sl2 > 0.f;
-        // masked tiles keep their scores pre-scaled (masked: -inf) in sr; interior ones raw
         float mx;
         {
             float t[8];
@@ -451,14 +448,13 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
             if (interior) mx *= sl2;
         }
-        // lazy rescale per row; this group's O (in TMEM) is rescaled for the whole warp when any
-        // row needs it, once the group's previous P . V (tile j - 2) has landed, each lane by its
-        // own factor
+        // lazy rescale per row; O_X (in TMEM) is rescaled for the whole warp when any row needs
+        // it, once P_X(j-1) . V_(j-1) has landed, each lane by its own factor
         const bool grow = mx > m + kLazyRescale;
         const bool scale_o = grow && m != -INFINITY;
         const float a = scale_o ? tc05::fast_exp2(m - mx) : 1.f;
-        if (j >= 2 && __any_sync(0xffffffffu, scale_o)) {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[g], ((j - 2) >> 1) & 1))) {
+        if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[X], (j - 1) & 1))) {
                 ok = false;
                 break;
             }
@@ -478,7 +474,7 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             m = mx;
         }
         const float ms = m == -INFINITY ? 0.f : m;
-        // P_j = 2^(v * mul - m) in one FFMA and one ex2 (interior: v raw, mul = scale; masked: v
+        // P = 2^(v * mul - m) in one FFMA and one ex2 (interior: v raw, mul = scale; masked: v
         // pre-scaled, mul = 1); key c at column c / 2 of S buffer sb, over this lane's own scores
         const float mul = interior ? sl2 : 1.f;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -496,7 +492,8 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             tc05::st16(sa + hq * 16, pw);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero them
+        // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero
+        // them (both groups write the same zeros; each P . V waits only for its own group's)
         if (key0 + BN > L || okmask != 0xF) {
             unsigned char* vt = smem + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
             for (int e = r; e < BN * NBOX * 8; e += 128) {
@@ -512,40 +509,25 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
         mbar_arrive(&p_full[sb]);
     }
     griddep_launch_dependents();
-    // merge the groups' states of row r: each O_g scaled by 2^(m_g - M), the normalisers alike;
-    // group g writes dims [g D/2, (g + 1) D/2)
-    red[g * 256 + r] = m;
-    red[g * 256 + 128 + r] = l;
     const bool all_ok = tc05::bar_and(2, C::NSW * 32, ok);
-    const float m0 = red[r], l0 = red[128 + r], m1 = red[256 + r], l1 = red[384 + r];
-    const float M = fmaxf(m0, m1);
-    const float f0 = m0 == -INFINITY ? 0.f : tc05::fast_exp2(m0 - M);
-    const float f1 = m1 == -INFINITY ? 0.f : tc05::fast_exp2(m1 - M);
-    const float den = f0 * l0 + f1 * l1;
-    const float inv = den > 0.f ? 1.f / den : 0.f;
     const bool done = all_ok && mbar_wait_bounded(o_final, 0);
     if (__all_sync(0xffffffffu, done)) {
         tc05::fence_after();
-        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + g * DH;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D;
 #pragma unroll
-        for (int c0 = 0; c0 < DH; c0 += 32) {
-            uint32_t x0[32], x1[32];
-            tc05::ld32(lane_addr + C::O_COL + g * DH + c0, x0);
-            tc05::ld32(lane_addr + C::O_COL + D + g * DH + c0, x1);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc05::ld32(o_addr + c0, o);
             tc05::wait_ld();
             if (valid) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i)  // a group that saw no tile never wrote its O: select it out
-                    v[i] = ((f0 != 0.f ? f0 * __uint_as_float(x0[i]) : 0.f) +
-                            (f1 != 0.f ? f1 * __uint_as_float(x1[i]) : 0.f)) * inv;
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
                     uint4 u;
-                    u.x = pack2<T>(v[i], v[i + 1]);
-                    u.y = pack2<T>(v[i + 2], v[i + 3]);
-                    u.z = pack2<T>(v[i + 4], v[i + 5]);
-                    u.w = pack2<T>(v[i + 6], v[i + 7]);
+                    u.x = pack2<T>(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
+                    u.y = pack2<T>(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                    u.z = pack2<T>(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
+                    u.w = pack2<T>(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
                     *reinterpret_cast<uint4*>(orow + c0 + i) = u;
                 }
             }
