@@ -98,6 +98,18 @@ def _kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def _launch_key(args, wl, rp) -> str:
+    """Name of the profiled launch: the workload plus whatever changes the kernel or its bytes."""
+    key = wl.name
+    if args.kv == "fp8":
+        key += "+e4m3"
+    if rp.partition_tokens != wl.partition_tokens:
+        key += f"+p{rp.partition_tokens}"
+    if args.kernel != "auto":
+        key += f"+{args.kernel}"
+    return key
+
+
 def _profiled_traffic(workload: str):
     """dram bytes per launch from a committed ncu summary, if taken on this kernel source."""
     d = os.path.join(ROOT, "profiles")
@@ -344,7 +356,7 @@ def run_ours(args, ws, rank, local):
         "seq_steps_per_s": seq_steps,
         "pct_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _profiled_traffic(wl.name),
+                     "frac": achieved / peak, "traffic": _profiled_traffic(_launch_key(args, wl, rp)),
                      "kernel": f"pa_decode ({args.kernel} partition + merge)", "peak_kind": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
