@@ -325,6 +325,8 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
 #pragma unroll
                 for (int X = 0; X < 2; ++X) {
                     const int j = js[X];
+                    // kv_full of tile j cannot move on before this S is issued (its refill needs both
+                    // tiles' P . V of tile j), so its phase parity is unambiguous here
                     if (j < n_kv && j < jp[X] + NSB && tc05::test_wait(&kv_full[j % STAGES], (j / STAGES) & 1)) {
                         tc05::fence_after();
                         const uint32_t kb = sbase + C::KV_OFF + (j % STAGES) * C::STAGE_BYTES;
@@ -341,6 +343,7 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
                         progressed = true;
                     }
                     const int t = jp[X];
+                    // P_X(t + NSB) needs S_X(t + NSB), which waits for this P . V: at most one phase ahead
                     if (t < js[X] && tc05::test_wait(&p_full[X * NSB + t % NSB], (t / NSB) & 1)) {
                         tc05::fence_after();
                         const int st = t % STAGES;
@@ -409,6 +412,8 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
     for (int j = 0; j < n_kv; ++j) {
         const int st = j % STAGES, sb = X * NSB + j % NSB;
         // decisions that guard a tcgen05.ld / st are warp-uniform (those are .sync.aligned)
+        // neither can run two phases ahead: tile j + STAGES is loaded, and S_X(j + NSB) issued,
+        // only after this thread's P_Xj has been consumed
         const bool got = mbar_wait_bounded(&kv_full[st], (j / STAGES) & 1) && mbar_wait_bounded(&s_full[sb], (j / NSB) & 1);
         if (!__all_sync(0xffffffffu, got)) {
             ok = false;
@@ -454,6 +459,8 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
         const bool scale_o = grow && m != -INFINITY;
         const float a = scale_o ? tc05::fast_exp2(m - mx) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
+            // o_ready[X] counts tile X's P . V in order: the one of tile j needs this thread's P_Xj,
+            // and the one of tile j - 2 completed before S_Xj (issued after it)
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&o_ready[X], (j - 1) & 1))) {
                 ok = false;
                 break;
