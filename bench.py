@@ -501,7 +501,7 @@ def run_op(args, local):
                               "frac": alg / (ms / 1e3) / 1e9 / peak, "alg_bytes_per_launch": alg,
                               "peak_kind": f"{peak_kind} hbm_gbs"})
     elif args.op == "copy":
-        N, Hkv, b, D, L, n = 4096, 8, 16, 128, 32, 64
+        N, Hkv, b, D, L, n = 4096, 8, 16, 128, args.copy_layers, args.copy_pairs
         kps = [torch.randn((N, Hkv, b, D), device=dev).half() for _ in range(L)]
         vps = [torch.randn((N, Hkv, b, D), device=dev).half() for _ in range(L)]
         perm = torch.randperm(N, device=dev)
@@ -592,6 +592,8 @@ def main():
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
     ap.add_argument("--kv", default="native", choices=["native", "fp8"], help="KV cache storage (fp8 = E4M3)")
     ap.add_argument("--partition", type=int, default=0, help="decode partition tokens (0: the workload's)")
+    ap.add_argument("--copy-layers", type=int, default=32, help="--op copy: layers (pools of 4096 blocks each)")
+    ap.add_argument("--copy-pairs", type=int, default=64, help="--op copy: copy-on-write pairs")
     ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc05"], help="--op prefill kernel")
     ap.add_argument("--prefill-dtype", default="bf16", choices=["f16", "bf16"], help="--op prefill storage dtype")
     ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host", "prefill"],
