@@ -154,15 +154,20 @@ struct MmaCfg {
 #endif
     static constexpr int RING_BYTES = NW * STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = RING_BYTES;
-    static constexpr int TBL_OFF = BAR_OFF + NW * STAGES * 8;
+    static constexpr int BAR_END = BAR_OFF + NW * STAGES * 8;
     static constexpr int KSTEPS = D / 16;
     static constexpr int RED_BYTES = NW * G * (D + 2) * 4;
-    static_assert(RED_BYTES <= RING_BYTES, "merge scratch aliases the ring");
+    static_assert(RED_BYTES <= RING_BYTES, "merge scratch may alias the ring");
     static_assert(G >= 1 && G <= 8, "query group on the N = 8 side");
     static_assert(!F8 || KSTEPS % 2 == 0, "FP8 fragments come in pairs of k-steps");
+    // With one KV head per CTA the warps' merge scratch aliases the ring; with two, the ring is
+    // still streaming the second head while the first is merged, so the scratch has its own
+    // region ahead of the table.
+    static constexpr int red_off(int heads_per_cta) { return heads_per_cta > 1 ? BAR_END : 0; }
+    static constexpr int tbl_off(int heads_per_cta) { return BAR_END + (heads_per_cta > 1 ? RED_BYTES : 0); }
     // + 1 KiB so the ring can be aligned to 1024 bytes for the 128-byte swizzle
-    static constexpr size_t smem_bytes(int table_entries) {
-        return 1024 + static_cast<size_t>(TBL_OFF) + static_cast<size_t>(table_entries) * 4;
+    static constexpr size_t smem_bytes(int table_entries, int heads_per_cta) {
+        return 1024 + static_cast<size_t>(tbl_off(heads_per_cta)) + static_cast<size_t>(table_entries) * 4;
     }
 };
 
@@ -185,20 +190,24 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-byte aligned ring
 
     griddep_wait();
-    const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+    const int part = blockIdx.x, s = blockIdx.z;
+    const int hpc = p.heads_per_cta;
+    const int kvh0 = blockIdx.y * hpc;
+    const int nh = min(hpc, p.hkv - kvh0);  // KV heads of this CTA, streamed back to back
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size, P = p.partition_tokens;
     const int cap = p.max_blocks * bs;
     int L = __ldg(p.seq_lens + s);
     if (L < 0 || L > cap) {
-        if (part == 0 && kvh == 0 && tid == 0) flag_error(p.err, PA_DEVERR_SEQLEN);
+        if (part == 0 && kvh0 == 0 && tid == 0) flag_error(p.err, PA_DEVERR_SEQLEN);
         L = L < 0 ? 0 : cap;
     }
     const int n_parts = (L + P - 1) / P;
-    T* out_rows = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + kvh * G) * D;
     if (L == 0) {
-        if (part == 0)
-            for (int i = tid; i < G * D; i += blockDim.x) out_rows[i] = Elt<T>::from_f32(0.f);
+        if (part == 0) {
+            T* out0 = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + kvh0 * G) * D;
+            for (int i = tid; i < nh * G * D; i += blockDim.x) out0[i] = Elt<T>::from_f32(0.f);
+        }
         return;
     }
     const int tok0 = part * P;
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
     const int tok1 = min(L, tok0 + P);
     const int n_tiles = (tok1 - tok0 + C::TILE - 1) / C::TILE;
 
-    int* tbl = reinterpret_cast<int*>(smem + C::TBL_OFF);
+    int* tbl = reinterpret_cast<int*>(smem + C::tbl_off(hpc));
     const int nblk = (tok1 - tok0 + bs - 1) / bs;
     const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks + tok0 / bs;
     for (int i = tid; i < nblk; i += blockDim.x) {
@@ -227,16 +236,19 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
 
     unsigned char* ring = smem + warp * STAGES * C::STAGE_BYTES;
     const int my_n = warp < n_tiles ? (n_tiles - warp + NW - 1) / NW : 0;
+    const int my_total = nh * my_n;  // this warp's tiles over all heads: one stream through its ring
 
-    auto issue = [&](int j) {
+    // tile jj of the stream: head jj / my_n, the warp's (jj % my_n)-th tile of the partition
+    auto issue = [&](int jj) {
+        const int u = jj / my_n, j = jj - u * my_n;
         const int i = warp + j * NW;
-        const int st = j % STAGES;
+        const int st = jj % STAGES;
         const int blk = tbl[(i * C::TILE) / bs];
         if (blk < 0) {
             mbar_arrive_expect_tx(&bars[st], 0);
             return;
         }
-        const int row = (blk * p.hkv + kvh) * bs + (i * C::TILE) % bs;
+        const int row = (blk * p.hkv + kvh0 + u) * bs + (i * C::TILE) % bs;
         unsigned char* dst = ring + st * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[st], 2 * C::TILE_BYTES);
 #pragma unroll
@@ -246,252 +258,290 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         }
     };
     if (lane == 0)
-        for (int j = 0; j < STAGES && j < my_n; ++j) issue(j);
+        for (int jj = 0; jj < STAGES && jj < my_total; ++jj) issue(jj);
 
-    // ---- query fragments (B operand of the score MMA): lane (g, t) holds
-    // Q[head g][k0 + 2t, +1] and Q[head g][k0 + 8 + 2t, +1]; heads >= G are zero.
     const int g = lane >> 2, t = lane & 3;
-    uint32_t qb[KSTEPS][2];
-    {
-        const T* qrow = static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.hq + kvh * G + g) * D;
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-            if (g < G) {
-                if constexpr (F8) {
-                    // dims 4t..4t+3 of this 16-dim step, matching the K fragment below
-                    const T* q4 = qrow + ks * 16 + 4 * t;
-                    qb[ks][0] = to_h2<T>(q4[0], q4[1]);
-                    qb[ks][1] = to_h2<T>(q4[2], q4[3]);
-                } else {
-                    qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 2 * t));
-                    qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + 2 * t));
-                }
-            } else {
-                qb[ks][0] = 0u;
-                qb[ks][1] = 0u;
-            }
-        }
-    }
-    // ---- output accumulators O^T: acc[mt] = {O[h0][dim mt*16+g], O[h1][..], O[h0][dim mt*16+g+8], O[h1][..]}
-    // with h0 = 2t, h1 = 2t + 1
-    float acc[KSTEPS][4];
-#pragma unroll
-    for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const float sl2 = F8 ? p.scale_log2 * __ldg(p.k_scale + kvh) : p.scale_log2;
-
     // ldmatrix addressing: lane provides row (lane & 7) of matrix (lane >> 3)
     const int lm = lane >> 3, lr = lane & 7;
-
-    for (int j = 0; j < my_n; ++j) {
-        const int st = j % STAGES;
-        if (!mbar_wait_bounded(&bars[st], (j / STAGES) & 1)) {
-            if (lane == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
-            for (int r = j + 1; r < my_n && r < j + STAGES; ++r) mbar_wait_bounded(&bars[r % STAGES], (r / STAGES) & 1);
-            break;
-        }
-        const int i = warp + j * NW;
-        const int nv = min(C::TILE, tok1 - (tok0 + i * C::TILE));
-        const bool present = tbl[(i * C::TILE) / bs] >= 0;
-        unsigned char* kt = ring + st * C::STAGE_BYTES;
-        unsigned char* vt = kt + C::TILE_BYTES;
-        if (present) {
-            // ---- scores S^T = K Q^T (16 tokens x 8 heads)
-            // two accumulators (even / odd k-steps) halve the chain of dependent MMAs
-            float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t kbase = smem_u32(kt);
-            const int krow = lr + (lm & 1) * 8;
-            if constexpr (F8) {
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ks += 2) {
-                    uint32_t r[4];
-                    ldsm_x4(kbase + swz(lr + (lm & 1) * 8, ks + (lm >> 1)), r);
-                    const uint32_t a0[4] = {e4m3x2_to_h2(r[0]), e4m3x2_to_h2(r[1]), e4m3x2_to_h2(r[0] >> 16),
-                                            e4m3x2_to_h2(r[1] >> 16)};
-                    const uint32_t a1[4] = {e4m3x2_to_h2(r[2]), e4m3x2_to_h2(r[3]), e4m3x2_to_h2(r[2] >> 16),
-                                            e4m3x2_to_h2(r[3] >> 16)};
-                    mma16816<TM>(sc, a0, qb[ks][0], qb[ks][1]);
-                    mma16816<TM>(sc2, a1, qb[ks + 1][0], qb[ks + 1][1]);
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
-                    uint32_t a[4];
-                    ldsm_x4(kbase + swz(krow, ks * 2 + (lm >> 1)), a);
-                    mma16816<TM>((ks & 1) ? sc2 : sc, a, qb[ks][0], qb[ks][1]);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
-            // sc = {S[tok g][h0], S[tok g][h1], S[tok g+8][h0], S[tok g+8][h1]}
-            const bool v0 = g < nv, v1 = g + 8 < nv;
-            sc[0] = v0 ? sc[0] * sl2 : -INFINITY;
-            sc[1] = v0 ? sc[1] * sl2 : -INFINITY;
-            sc[2] = v1 ? sc[2] * sl2 : -INFINITY;
-            sc[3] = v1 ? sc[3] * sl2 : -INFINITY;
-            float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            if (mx0 > m0 + kLazyRescale) {
-                const float a0 = exp2f(m0 - mx0);
-                l0 *= a0;
-#pragma unroll
-                for (int mt = 0; mt < KSTEPS; ++mt) {
-                    acc[mt][0] *= a0;
-                    acc[mt][2] *= a0;
-                }
-                m0 = mx0;
-            }
-            if (mx1 > m1 + kLazyRescale) {
-                const float a1 = exp2f(m1 - mx1);
-                l1 *= a1;
-#pragma unroll
-                for (int mt = 0; mt < KSTEPS; ++mt) {
-                    acc[mt][1] *= a1;
-                    acc[mt][3] *= a1;
-                }
-                m1 = mx1;
-            }
-            const float p0 = exp2f(sc[0] - m0), p1 = exp2f(sc[1] - m1);
-            const float p2 = exp2f(sc[2] - m0), p3 = exp2f(sc[3] - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // P^T operand: transpose the 8x8 (token x head) halves
-            const uint32_t pb0 = movmatrix_t(pack2<TM>(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack2<TM>(p2, p3));
-            if (nv < C::TILE) {
-                // unwritten slots of the tail may hold anything (NaN * 0 = NaN): zero those V rows
-                for (int e = lane; e < (C::TILE - nv) * C::CHUNKS; e += 32) {
-                    const int r = nv + e / C::CHUNKS, c = e % C::CHUNKS;
-                    *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                __syncwarp();
-            }
-            // ---- O^T += V^T P^T
-            const uint32_t vbase = smem_u32(vt);
-            const int vrow = lr + (lm >> 1) * 8;
-            if constexpr (F8) {
-#pragma unroll
-                for (int mt = 0; mt < KSTEPS; mt += 2) {
-                    uint32_t r[4];
-                    ldsm_x4_t(vbase + swz(lr + (lm & 1) * 8, mt + (lm >> 1)), r);
-                    // r[i] bytes: (tok 2t, dim 2g), (tok 2t, dim 2g+1), (tok 2t+1, dim 2g), (tok 2t+1, dim 2g+1)
-                    const uint32_t a0[4] = {e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x20u)),
-                                            e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x31u)),
-                                            e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x20u)),
-                                            e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x31u))};
-                    const uint32_t a1[4] = {e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x20u)),
-                                            e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x31u)),
-                                            e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x20u)),
-                                            e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x31u))};
-                    mma16816<TM>(acc[mt], a0, pb0, pb1);
-                    mma16816<TM>(acc[mt + 1], a1, pb0, pb1);
-                }
-            } else {
-#pragma unroll
-                for (int mt = 0; mt < KSTEPS; ++mt) {
-                    uint32_t a[4];
-                    ldsm_x4_t(vbase + swz(vrow, mt * 2 + (lm & 1)), a);
-                    mma16816<TM>(acc[mt], a, pb0, pb1);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && j + STAGES < my_n) {
-            fence_proxy_async_smem();  // order this warp's shared accesses before the next async copy
-            issue(j + STAGES);
-        }
-    }
-
-    griddep_launch_dependents();
-
-    // ---- normalisers: sum over the 8 token rows held by lanes with the same t
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-
-    // ---- merge the warps through shared memory (aliases the ring)
-    __syncthreads();
-    float* red_m = reinterpret_cast<float*>(smem);
+    float* red_m = reinterpret_cast<float*>(smem + C::red_off(hpc));
     float* red_l = red_m + NW * G;
     float* red_acc = red_l + NW * G;
     const int h0 = 2 * t, h1 = 2 * t + 1;
-    if (g == 0) {
-        if (h0 < G) {
-            red_m[warp * G + h0] = m0;
-            red_l[warp * G + h0] = l0;
-        }
-        if (h1 < G) {
-            red_m[warp * G + h1] = m1;
-            red_l[warp * G + h1] = l1;
-        }
-    }
-    // MMA rows g and g+8 are dims g and g+8 of the 16-dim tile (FP8: dims 2g, 2g+1)
-    const int dA = F8 ? 2 * g : g, dB = F8 ? 2 * g + 1 : g + 8;
-    const float vs = F8 ? __ldg(p.v_scale + kvh) : 1.f;
-#pragma unroll
-    for (int mt = 0; mt < KSTEPS; ++mt) {
-        if (h0 < G) {
-            red_acc[(warp * G + h0) * D + mt * 16 + dA] = acc[mt][0] * vs;
-            red_acc[(warp * G + h0) * D + mt * 16 + dB] = acc[mt][2] * vs;
-        }
-        if (h1 < G) {
-            red_acc[(warp * G + h1) * D + mt * 16 + dA] = acc[mt][1] * vs;
-            red_acc[(warp * G + h1) * D + mt * 16 + dB] = acc[mt][3] * vs;
-        }
-    }
-    __syncthreads();
+    bool aborted = false;
 
-    const bool direct = n_parts == 1;
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        const int hh = idx / D, d = idx - hh * D;
-        float M = -INFINITY;
+    for (int u = 0; u < nh; ++u) {
+        const int kvh = kvh0 + u;
+        T* out_rows = static_cast<T*>(p.out) + (static_cast<size_t>(s) * p.hq + kvh * G) * D;
+        // ---- query fragments (B operand of the score MMA): lane (g, t) holds
+        // Q[head g][k0 + 2t, +1] and Q[head g][k0 + 8 + 2t, +1]; heads >= G are zero.
+        uint32_t qb[KSTEPS][2];
+        {
+            const T* qrow = static_cast<const T*>(p.q) + (static_cast<size_t>(s) * p.hq + kvh * G + g) * D;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + hh]);
-        float num = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float f = exp2f(red_m[w * G + hh] - M);
-                num = fmaf(f, red_acc[(w * G + hh) * D + d], num);
-                den = fmaf(f, red_l[w * G + hh], den);
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                if (g < G) {
+                    if constexpr (F8) {
+                        // dims 4t..4t+3 of this 16-dim step, matching the K fragment below
+                        const T* q4 = qrow + ks * 16 + 4 * t;
+                        qb[ks][0] = to_h2<T>(q4[0], q4[1]);
+                        qb[ks][1] = to_h2<T>(q4[2], q4[3]);
+                    } else {
+                        qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 2 * t));
+                        qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + 2 * t));
+                    }
+                } else {
+                    qb[ks][0] = 0u;
+                    qb[ks][1] = 0u;
+                }
             }
         }
-        if (direct) {
-            out_rows[idx] = Elt<T>::from_f32(den > 0.f ? num / den : 0.f);
-        } else {
-            const size_t row = (static_cast<size_t>(s) * p.hq + kvh * G + hh) * p.max_partitions + part;
-            p.ws_acc[row * D + d] = num;
-            if (d == 0) {
-                p.ws_ml[row * 2] = M;
-                p.ws_ml[row * 2 + 1] = den;
+        // ---- output accumulators O^T: acc[mt] = {O[h0][dim mt*16+g], O[h1][..], O[h0][dim mt*16+g+8], O[h1][..]}
+        // with h0 = 2t, h1 = 2t + 1
+        float acc[KSTEPS][4];
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const float sl2 = F8 ? p.scale_log2 * __ldg(p.k_scale + kvh) : p.scale_log2;
+
+        for (int j = 0; j < my_n && !aborted; ++j) {
+            const int jj = u * my_n + j;
+            const int st = jj % STAGES;
+            if (!mbar_wait_bounded(&bars[st], (jj / STAGES) & 1)) {
+                if (lane == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
+                for (int r = jj + 1; r < my_total && r < jj + STAGES; ++r)
+                    mbar_wait_bounded(&bars[r % STAGES], (r / STAGES) & 1);
+                aborted = true;
+                break;
+            }
+            const int i = warp + j * NW;
+            const int nv = min(C::TILE, tok1 - (tok0 + i * C::TILE));
+            const bool present = tbl[(i * C::TILE) / bs] >= 0;
+            unsigned char* kt = ring + st * C::STAGE_BYTES;
+            unsigned char* vt = kt + C::TILE_BYTES;
+            if (present) {
+                // ---- scores S^T = K Q^T (16 tokens x 8 heads)
+                // two accumulators (even / odd k-steps) halve the chain of dependent MMAs
+                float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t kbase = smem_u32(kt);
+                const int krow = lr + (lm & 1) * 8;
+                if constexpr (F8) {
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ks += 2) {
+                        uint32_t r[4];
+                        ldsm_x4(kbase + swz(lr + (lm & 1) * 8, ks + (lm >> 1)), r);
+                        const uint32_t a0[4] = {e4m3x2_to_h2(r[0]), e4m3x2_to_h2(r[1]), e4m3x2_to_h2(r[0] >> 16),
+                                                e4m3x2_to_h2(r[1] >> 16)};
+                        const uint32_t a1[4] = {e4m3x2_to_h2(r[2]), e4m3x2_to_h2(r[3]), e4m3x2_to_h2(r[2] >> 16),
+                                                e4m3x2_to_h2(r[3] >> 16)};
+                        mma16816<TM>(sc, a0, qb[ks][0], qb[ks][1]);
+                        mma16816<TM>(sc2, a1, qb[ks + 1][0], qb[ks + 1][1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                        uint32_t a[4];
+                        ldsm_x4(kbase + swz(krow, ks * 2 + (lm >> 1)), a);
+                        mma16816<TM>((ks & 1) ? sc2 : sc, a, qb[ks][0], qb[ks][1]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
+                // sc = {S[tok g][h0], S[tok g][h1], S[tok g+8][h0], S[tok g+8][h1]}
+                const bool v0 = g < nv, v1 = g + 8 < nv;
+                sc[0] = v0 ? sc[0] * sl2 : -INFINITY;
+                sc[1] = v0 ? sc[1] * sl2 : -INFINITY;
+                sc[2] = v1 ? sc[2] * sl2 : -INFINITY;
+                sc[3] = v1 ? sc[3] * sl2 : -INFINITY;
+                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                if (mx0 > m0 + kLazyRescale) {
+                    const float a0 = exp2f(m0 - mx0);
+                    l0 *= a0;
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; ++mt) {
+                        acc[mt][0] *= a0;
+                        acc[mt][2] *= a0;
+                    }
+                    m0 = mx0;
+                }
+                if (mx1 > m1 + kLazyRescale) {
+                    const float a1 = exp2f(m1 - mx1);
+                    l1 *= a1;
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; ++mt) {
+                        acc[mt][1] *= a1;
+                        acc[mt][3] *= a1;
+                    }
+                    m1 = mx1;
+                }
+                const float p0 = exp2f(sc[0] - m0), p1 = exp2f(sc[1] - m1);
+                const float p2 = exp2f(sc[2] - m0), p3 = exp2f(sc[3] - m1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // P^T operand: transpose the 8x8 (token x head) halves
+                const uint32_t pb0 = movmatrix_t(pack2<TM>(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack2<TM>(p2, p3));
+                if (nv < C::TILE) {
+                    // unwritten slots of the tail may hold anything (NaN * 0 = NaN): zero those V rows
+                    for (int e = lane; e < (C::TILE - nv) * C::CHUNKS; e += 32) {
+                        const int r = nv + e / C::CHUNKS, c = e % C::CHUNKS;
+                        *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
+                // ---- O^T += V^T P^T
+                const uint32_t vbase = smem_u32(vt);
+                const int vrow = lr + (lm >> 1) * 8;
+                if constexpr (F8) {
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; mt += 2) {
+                        uint32_t r[4];
+                        ldsm_x4_t(vbase + swz(lr + (lm & 1) * 8, mt + (lm >> 1)), r);
+                        // r[i] bytes: (tok 2t, dim 2g), (tok 2t, dim 2g+1), (tok 2t+1, dim 2g), (tok 2t+1, dim 2g+1)
+                        const uint32_t a0[4] = {e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x20u)),
+                                                e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x31u)),
+                                                e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x20u)),
+                                                e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x31u))};
+                        const uint32_t a1[4] = {e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x20u)),
+                                                e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x31u)),
+                                                e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x20u)),
+                                                e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x31u))};
+                        mma16816<TM>(acc[mt], a0, pb0, pb1);
+                        mma16816<TM>(acc[mt + 1], a1, pb0, pb1);
+                    }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; ++mt) {
+                        uint32_t a[4];
+                        ldsm_x4_t(vbase + swz(vrow, mt * 2 + (lm & 1)), a);
+                        mma16816<TM>(acc[mt], a, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && jj + STAGES < my_total) {
+                fence_proxy_async_smem();  // order this warp's shared accesses before the next async copy
+                issue(jj + STAGES);
             }
         }
-    }
+        if (u + 1 == nh) griddep_launch_dependents();
 
+        // ---- normalisers: sum over the 8 token rows held by lanes with the same t
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+
+        // ---- merge the warps through shared memory (aliasing the ring when one head per CTA)
+        __syncthreads();
+        if (g == 0) {
+            if (h0 < G) {
+                red_m[warp * G + h0] = m0;
+                red_l[warp * G + h0] = l0;
+            }
+            if (h1 < G) {
+                red_m[warp * G + h1] = m1;
+                red_l[warp * G + h1] = l1;
+            }
+        }
+        // MMA rows g and g+8 are dims g and g+8 of the 16-dim tile (FP8: dims 2g, 2g+1)
+        const int dA = F8 ? 2 * g : g, dB = F8 ? 2 * g + 1 : g + 8;
+        const float vs = F8 ? __ldg(p.v_scale + kvh) : 1.f;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+            if (h0 < G) {
+                red_acc[(warp * G + h0) * D + mt * 16 + dA] = acc[mt][0] * vs;
+                red_acc[(warp * G + h0) * D + mt * 16 + dB] = acc[mt][2] * vs;
+            }
+            if (h1 < G) {
+                red_acc[(warp * G + h1) * D + mt * 16 + dA] = acc[mt][1] * vs;
+                red_acc[(warp * G + h1) * D + mt * 16 + dB] = acc[mt][3] * vs;
+            }
+        }
+        __syncthreads();
+
+        const bool direct = n_parts == 1;
+        for (int idx = tid; idx < G * D; idx += blockDim.x) {
+            const int hh = idx / D, d = idx - hh * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + hh]);
+            float num = 0.f, den = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float f = exp2f(red_m[w * G + hh] - M);
+                    num = fmaf(f, red_acc[(w * G + hh) * D + d], num);
+                    den = fmaf(f, red_l[w * G + hh], den);
+                }
+            }
+            if (direct) {
+                out_rows[idx] = Elt<T>::from_f32(den > 0.f ? num / den : 0.f);
+            } else {
+                const size_t row = (static_cast<size_t>(s) * p.hq + kvh * G + hh) * p.max_partitions + part;
+                p.ws_acc[row * D + d] = num;
+                if (d == 0) {
+                    p.ws_ml[row * 2] = M;
+                    p.ws_ml[row * 2 + 1] = den;
+                }
+            }
+        }
+        // every thread leaves the merge before the next head's warps write the scratch, and a
+        // timeout anywhere ends the CTA after this head (uniform: read after the barrier)
+        if (u + 1 < nh) {
+            __shared__ int s_abort;
+            if (tid == 0) s_abort = 0;
+            __syncthreads();
+            if (aborted) s_abort = 1;
+            __syncthreads();
+            if (s_abort) break;
+        }
+    }
 }
 
 template <typename T, typename PE, int D, int G>
-cudaError_t launch_mma(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+cudaError_t launch_mma(const DecodeParams& p_in, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        cudaStream_t stream) {
     using C = MmaCfg<PE, D, G>;
-    const size_t smem = C::smem_bytes(p.partition_tokens / p.block_size);
+    DecodeParams p = p_in;
+    const int entries = p.partition_tokens / p.block_size;
     static int configured_for = -1;  // device on which the attribute was last set
+    static int cached_entries = -1, cached_hpc = 1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
         cudaError_t e = cudaFuncSetAttribute(decode_partition_mma<T, PE, D, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(C::smem_bytes(8192 / 16)));
+                                             static_cast<int>(C::smem_bytes(8192 / 16, 2)));
         if (e != cudaSuccess) return e;
         configured_for = dev;
+        cached_entries = -1;
     }
-    dim3 grid(p.max_partitions, p.hkv, p.batch);
+    if (cached_entries != entries) {
+        // two KV heads per CTA (table staged once, the ring streaming on into the second head)
+        // when the merge scratch it needs of its own costs no resident CTA
+        int occ1 = 0, occ2 = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, decode_partition_mma<T, PE, D, G>,
+                                                                      C::NW * 32, C::smem_bytes(entries, 1));
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, decode_partition_mma<T, PE, D, G>, C::NW * 32,
+                                                              C::smem_bytes(entries, 2));
+        if (e != cudaSuccess) return e;
+        cached_hpc = occ2 >= occ1 ? 2 : 1;
+        cached_entries = entries;
+    }
+#ifdef PA_MMA_HEADS
+    p.heads_per_cta = PA_MMA_HEADS;  // build-time override (tuning sweeps)
+#else
+    p.heads_per_cta = p.hkv >= 2 ? cached_hpc : 1;
+#endif
+    const size_t smem = C::smem_bytes(entries, p.heads_per_cta);
+    dim3 grid(p.max_partitions, (p.hkv + p.heads_per_cta - 1) / p.heads_per_cta, p.batch);
     cudaError_t e =
         launch_pdl(decode_partition_mma<T, PE, D, G>, grid, dim3(C::NW * 32), smem, stream, p, kmap, vmap);
     if (e != cudaSuccess || p.max_partitions <= 1) return e;

@@ -39,6 +39,7 @@ struct DecodeParams {
     int kernel;                 // pa_decode_kernel choice (PA_DECODE_AUTO / _SIMT / _MMA)
     const float* k_scale;       // FP8 pools: [Hkv] scale of K codes (else null)
     const float* v_scale;       // FP8 pools: [Hkv] scale of V codes (else null)
+    int heads_per_cta;          // tensor-core kernel: KV heads one CTA streams back to back (1 or 2)
 };
 
 // Everything one pa_prefill call needs on the device.
