@@ -4,7 +4,7 @@
 the end of that block, because a block's K/V depend on every earlier token;
 production engines hash the chain of block contents instead of keeping the
 tuples, and the key must also cover whatever else changes the activations
-(model revision, adapter, multimodal inputs).  [P2] "Prefix sharing" says
+(model revision, adapter, multimodal inputs).  [P2] "4. Prefix sharing и copy-on-write" says
 the same of vLLM's automatic prefix caching (a block hashed by its tokens
 and the hashes of the blocks before it); [P4] "Prefix sharing
 (copy-on-write intuition)" likewise (block contents plus prefix identity).
