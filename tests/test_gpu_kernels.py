@@ -153,6 +153,10 @@ CASES = [
     (16, 2, 256, 16, [1, 200, 900], 0),
     (16, 2, 256, 32, [64, 513], 256),
     (8, 4, 128, 16, [16 * 37 + 5, 8], 0),
+    (12, 3, 128, 16, [100, 700, 1], 0),                 # odd Hkv: the last CTA of a head pair has one head
+    (8, 1, 128, 64, [1, 65, 900], 0),                   # MQA, b = 64
+    (32, 8, 128, 256, [1, 255, 256, 257, 1500], 0),     # b = 256: one block per half partition
+    (16, 4, 64, 128, [300, 1025], 0),
 ]
 
 

@@ -89,6 +89,10 @@ CASES = [
     (4, 1, 64, 16, [16, 17, 15], [16, 17, 15]),
     (32, 4, 128, 16, [47, 8], [47, 8]),
     (8, 1, 256, 16, [33], [2]),
+    (8, 2, 128, 64, [300, 64], [150, 64]),             # b = 64
+    (4, 4, 64, 256, [600], [600]),                      # b = 256, G = 1: 600 chunk rows over 3 CTAs
+    (4, 4, 128, 16, [700], [700]),                      # G = 1, a whole 256-row CTA plus a ragged one
+    (6, 3, 128, 16, [200, 90], [100, 90]),              # odd Hkv
 ]
 
 
