@@ -107,6 +107,8 @@ def _launch_key(args, wl, rp) -> str:
         key += f"+p{rp.partition_tokens}"
     if args.kernel != "auto":
         key += f"+{args.kernel}"
+    if not rp.fused:
+        key += "+unfused"
     return key
 
 
@@ -189,12 +191,15 @@ def _kv_bytes(wl, lens, elt=None) -> int:
     return int(np.sum(np.asarray(lens, dtype=np.int64))) * 2 * wl.Hkv * wl.D * (wl.elt if elt is None else elt)
 
 
-def _alg_bytes_decode(wl, plan, kv_elt=None) -> int:
+def _alg_bytes_decode(wl, plan, kv_elt=None, fused=False) -> int:
     """Algorithmic bytes of one pa_decode launch: K/V history + q + out + block
-    tables + lengths (scratch traffic of the split is not algorithmic)."""
+    tables + lengths (scratch traffic of the split is not algorithmic).  A fused
+    pa_decode_append also reads each sequence's new K/V row and its slot and
+    writes the row into the pool."""
     B = len(plan.uids)
     tbl = int(np.sum((np.asarray(plan.lens, dtype=np.int64) + wl.b - 1) // wl.b)) * 4
-    return _kv_bytes(wl, plan.lens, kv_elt) + 2 * B * wl.Hq * wl.D * wl.elt + tbl + 4 * B
+    extra = (4 * B * wl.Hkv * wl.D * wl.elt + 8 * B) if fused else 0
+    return _kv_bytes(wl, plan.lens, kv_elt) + 2 * B * wl.Hq * wl.D * wl.elt + tbl + 4 * B + extra
 
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
@@ -283,7 +288,7 @@ def run_ours(args, ws, rank, local):
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
         wl.layers = min(wl.layers, args.layers)
-    rp = Replay(wl, device=dev, kv=args.kv, partition_tokens=args.partition or None)
+    rp = Replay(wl, device=dev, kv=args.kv, partition_tokens=args.partition or None, fused=not args.unfused)
     rp.run_setup()
     torch.cuda.synchronize()
 
@@ -314,12 +319,9 @@ def run_ours(args, ws, rank, local):
             api.pa_copy_blocks(rp.k_pools, rp.v_pools, ds.pairs)
             launches += 1
         for li in range(nL):
-            rp.append(li, ds.k_new[li], ds.v_new[li], ds.slots)
-            a, b = ev_dec[j * nL + li]
-            a.record(stream)
-            rp.decode(li, outs[li], ds.q[li], ds.tables, ds.lens, wsbuf)
-            b.record(stream)
-            launches += 2 + (1 if wsbuf.numel() else 0)
+            launches += rp.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables,
+                                      ds.lens, wsbuf, events=ev_dec[j * nL + li])
+            launches += 1 if wsbuf.numel() else 0
     t_end.record(stream)
     torch.cuda.synchronize()
     _barrier(ws)
@@ -333,7 +335,8 @@ def run_ours(args, ws, rank, local):
     seq_steps = B * args.steps * ws / (dev_ms_max / 1e3)
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
     dec_avg = sum(dec_ms) / len(dec_ms)
-    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan, rp.kv_elt) for j in range(args.steps))
+    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan, rp.kv_elt, rp.fused)
+                          for j in range(args.steps))
     peak, peak_kind = _peaks()
     achieved = alg / (dec_avg / 1e3) / 1e9
     err = api.pa_get_device_error()
@@ -357,7 +360,9 @@ def run_ours(args, ws, rank, local):
         "pct_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(_launch_key(args, wl, rp)),
-                     "kernel": f"pa_decode ({args.kernel} partition + merge)", "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": (f"pa_decode_append ({args.kernel} partition with the step's append + merge)"
+                                if rp.fused else f"pa_decode ({args.kernel} partition + merge)"),
+                     "peak_kind": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
@@ -442,8 +447,7 @@ def run_e2e(args, wl, rp, dev, ws):
         h2d += host_in[j].numel() * wl.elt
         wsbuf = rp.workspace_for(B, stride)
         for li in range(nL):
-            rp.append(li, d_k[li], d_v[li], d_slots)
-            rp.decode(li, d_out[li], d_q[li], d_tables, d_lens, wsbuf)
+            rp.step_layer(li, d_out[li], d_q[li], d_k[li], d_v[li], d_slots, d_tables, d_lens, wsbuf)
         out_host.copy_(d_out, non_blocking=True)
         d2h += d_out.numel() * wl.elt
     t1.record(stream)
@@ -590,6 +594,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode step: separate append and decode launches instead of pa_decode_append")
     ap.add_argument("--kv", default="native", choices=["native", "fp8"], help="KV cache storage (fp8 = E4M3)")
     ap.add_argument("--partition", type=int, default=0, help="decode partition tokens (0: the workload's)")
     ap.add_argument("--copy-layers", type=int, default=32, help="--op copy: layers (pools of 4096 blocks each)")

@@ -64,7 +64,8 @@ typedef enum pa_dtype {
 } pa_dtype;
 
 /* Bits of the device error word (see pa_get_device_error). */
-#define PA_DEVERR_SLOT 1         /* pa_kv_append: slot >= num_blocks * b        */
+#define PA_DEVERR_SLOT 1         /* pa_kv_append: slot >= num_blocks * b;
+                                    pa_decode_append: slot not position L - 1's */
 #define PA_DEVERR_TABLE 2        /* pa_decode: table entry outside [0, num_blocks) */
 #define PA_DEVERR_SEQLEN 4       /* pa_decode: seq_len < 0 or > max_blocks * b  */
 #define PA_DEVERR_PAIR 8         /* pa_copy_blocks: src or dst outside the pool */
@@ -146,6 +147,33 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
                     const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
                     int head_dim, int block_size, float scale, int partition_tokens,
                     void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_decode_append -- pa_kv_append of each sequence's newest row followed by
+ * pa_decode, for the decode step where every sequence appends exactly one
+ * token ("25. Paged attention and prefix caching", "The paged cache": update
+ * writes the step's K/V, then attention reads the history including it).
+ *   k_new, v_new   [batch, Hkv, D] `dtype`, device: the rows of position
+ *                  seq_lens[s] - 1 (the newest) of sequence s.
+ *   slot_mapping   int64 [batch], device: the slot of that position, i.e.
+ *                  table[s][(L-1) / b] * b + (L-1) % b; negative: no row
+ *                  (give a negative slot for a sequence with L_s = 0).
+ *   Other arguments and the workspace as for pa_decode.
+ * The pools end bit for bit as after pa_kv_append, and the outputs equal
+ * pa_decode's.  fp16 / bf16 pools with the tensor-core kernel do both in one
+ * launch: the CTA whose partition holds position L - 1 writes the rows of its
+ * KV heads before it streams that position.  A slot that is not the table's
+ * slot of position L - 1 is skipped and flags PA_DEVERR_SLOT (its row is then
+ * not written).  fp32 pools, the CUDA-core kernel forced by
+ * pa_set_decode_kernel, or pools of 2^31 rows or more run pa_kv_append and
+ * then pa_decode (the slot is then not checked against the table).
+ */
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, void* k_pool, void* v_pool, int64_t num_blocks,
+                           const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                           int partition_tokens, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                           void* stream);
 
 /*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device

@@ -28,6 +28,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
                          _vp, _sz, _i32, _vp]),
+    "pa_decode_append": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                _i32, _f32, _i32, _vp, _sz, _i32, _vp]),
     "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                  _i32, _i32, _vp]),
     "pa_kv_append_fp8": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),

@@ -18,7 +18,7 @@ _TORCH_TO_ID = {torch.float32: DTYPE_IDS["f32"], torch.float16: DTYPE_IDS["f16"]
                 torch.bfloat16: DTYPE_IDS["bf16"]}
 
 __all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
-           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_set_prefill_kernel", "pa_get_device_error", "pa_status_string", "PagedKVError"]
+           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_set_prefill_kernel", "pa_decode_append", "pa_get_device_error", "pa_status_string", "PagedKVError"]
 
 
 def _stream(stream):
@@ -130,6 +130,34 @@ def pa_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, qstart, scale, ma
                          block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32),
                          _dev(qstart, "qstart", torch.int32), B, T, int(max_query_len), Hq, Hkv, D, b, float(scale),
                          _dtype_id(k_pool), _stream(stream)), "pa_prefill")
+
+
+def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables, seq_lens, scale,
+                     partition_tokens=0, workspace=None, stream=None) -> None:
+    """pa_kv_append of each sequence's newest row (k_new, v_new [B, Hkv, D] at
+    slot_mapping [B] int64, the slot of position seq_lens[s] - 1) followed by
+    pa_decode; one launch for fp16 / bf16 pools on the tensor-core kernel."""
+    lib = load()
+    B, Hq, D = q.shape
+    N, Hkv, b, D2 = k_pool.shape
+    if D2 != D or tuple(out.shape) != tuple(q.shape) or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("shape mismatch between q, out and the pools")
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D) or slot_mapping.shape != (B,):
+        raise ValueError("k_new, v_new must be [B, Hkv, D] and slot_mapping [B]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks] and seq_lens [B]")
+    dt = k_pool.dtype
+    ws_ptr, ws_bytes = C.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib.pa_decode_append(_dev(out, "out", dt), _dev(q, "q", dt), _dev(k_new, "k_new", dt),
+                               _dev(v_new, "v_new", dt), _dev(slot_mapping, "slot_mapping", torch.int64),
+                               _dev(k_pool, "k_pool", dt), _dev(v_pool, "v_pool", dt), N,
+                               _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                               _dev(seq_lens, "seq_lens", torch.int32), B, Hq, Hkv, D, b, float(scale),
+                               int(partition_tokens), ws_ptr, ws_bytes, _dtype_id(k_pool), _stream(stream)),
+          "pa_decode_append")
 
 
 def pa_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale, partition_tokens=0,

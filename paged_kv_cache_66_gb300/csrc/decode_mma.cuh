@@ -226,6 +226,32 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         }
         tbl[i] = e;
     }
+    if constexpr (!F8) {
+        // fused append: the partition holding position L - 1 writes that position's K/V rows
+        // of its heads before any of its copies is issued (the pool stores are fenced against
+        // the async proxy, and the barrier below orders them before the TMA loads)
+        if (p.new_slots != nullptr && tok1 == L) {
+            const int64_t slot = __ldg(p.new_slots + s);
+            if (slot >= 0) {
+                const int e = __ldg(trow + (L - 1) / bs - tok0 / bs);
+                if (e < 0 || e >= p.num_blocks || slot != static_cast<int64_t>(e) * bs + (L - 1) % bs) {
+                    if (tid == 0) flag_error(p.err, PA_DEVERR_SLOT);
+                } else {
+                    constexpr int VPR = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte vectors per row
+                    for (int x = tid; x < nh * 2 * VPR; x += blockDim.x) {
+                        const int u = x / (2 * VPR), kind = (x / VPR) & 1, v = x % VPR;
+                        const int h = kvh0 + u;
+                        const uint4* src = static_cast<const uint4*>(kind ? p.v_new : p.k_new) +
+                                           (static_cast<size_t>(s) * p.hkv + h) * VPR + v;
+                        uint4* dst = static_cast<uint4*>(const_cast<void*>(kind ? p.v_pool : p.k_pool)) +
+                                     ((static_cast<size_t>(e) * p.hkv + h) * bs + (L - 1) % bs) * VPR + v;
+                        *dst = __ldg(src);
+                    }
+                    fence_proxy_async_global();
+                }
+            }
+        }
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * STAGES;
     if (lane == 0) {
 #pragma unroll

@@ -168,10 +168,15 @@ size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int ma
     return ws_layout(batch, num_q_heads, head_dim, max_blocks, block_size, part).total;
 }
 
-pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
-                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
-                    int num_kv_heads, int head_dim, int block_size, float scale, int partition_tokens,
-                    void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+namespace {
+
+// pa_decode with, optionally, the fused append of each sequence's newest row (k_new, v_new,
+// new_slots non-null: tensor-core kernel only, the caller has checked that it applies)
+pa_status decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+                      const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, float scale, int partition_tokens,
+                      void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream, const void* k_new,
+                      const void* v_new, const int64_t* new_slots) {
     const int es = elt_size(dtype);
     if (es == 0 || batch < 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 ||
         head_dim <= 0 || block_size <= 0 || max_blocks <= 0 || num_blocks <= 0 || !std::isfinite(scale))
@@ -216,6 +221,9 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
     p.partition_tokens = part;
     p.max_partitions = ws.partitions < 1 ? 1 : ws.partitions;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.new_slots = new_slots;
     p.kernel = g_decode_kernel.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
@@ -224,6 +232,44 @@ pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_
         case PA_BF16: return from_cuda(pa::launch_decode_bf16(p, st));
         default: return PA_ERR_INVALID;
     }
+}
+
+}  // namespace
+
+pa_status pa_decode(void* out, const void* q, const void* k_pool, const void* v_pool, int64_t num_blocks,
+                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, float scale, int partition_tokens,
+                    void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+    return decode_impl(out, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, scale, partition_tokens, workspace, workspace_bytes, dtype,
+                       stream, nullptr, nullptr, nullptr);
+}
+
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, void* k_pool, void* v_pool, int64_t num_blocks,
+                           const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                           int partition_tokens, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                           void* stream) {
+    if (batch > 0 && (!k_new || !v_new || !slot_mapping || !al(k_new, 16) || !al(v_new, 16) || !al(slot_mapping, 8)))
+        return PA_ERR_INVALID;
+    const bool fuse = (dtype == PA_F16 || dtype == PA_BF16) && g_decode_kernel.load() != PA_DECODE_SIMT &&
+                      num_blocks > 0 && num_kv_heads > 0 && block_size > 0 &&
+                      static_cast<uint64_t>(num_blocks) * num_kv_heads * block_size < (1ull << 31);
+    if (!fuse) {
+        // the CUDA-core kernel writes nothing itself: the append kernel, then the decode
+        if (batch > 0) {
+            const pa_status st = pa_kv_append(k_new, v_new, k_pool, v_pool, slot_mapping, batch, num_blocks,
+                                              num_kv_heads, head_dim, block_size, dtype, stream);
+            if (st != PA_OK) return st;
+        }
+        return pa_decode(out, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens, batch, num_q_heads,
+                         num_kv_heads, head_dim, block_size, scale, partition_tokens, workspace, workspace_bytes,
+                         dtype, stream);
+    }
+    return decode_impl(out, q, k_pool, v_pool, num_blocks, block_tables, max_blocks, seq_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, scale, partition_tokens, workspace, workspace_bytes, dtype,
+                       stream, k_new, v_new, slot_mapping);
 }
 
 pa_status pa_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,

@@ -144,6 +144,11 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // be scheduled while the previous kernel of the stream drains; it waits for
 // that kernel (completion and memory) before touching any data, and signals
 // its own dependents once its remaining work no longer needs new CTAs.
+// orders this thread's generic-proxy global writes before later async-proxy (TMA) accesses
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

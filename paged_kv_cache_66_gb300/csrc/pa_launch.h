@@ -40,6 +40,11 @@ struct DecodeParams {
     const float* k_scale;       // FP8 pools: [Hkv] scale of K codes (else null)
     const float* v_scale;       // FP8 pools: [Hkv] scale of V codes (else null)
     int heads_per_cta;          // tensor-core kernel: KV heads one CTA streams back to back (1 or 2)
+    // fused append (16-bit pools, tensor-core kernel): the row of position seq_lens[s] - 1 of
+    // every sequence, written by the CTA that streams it (null: plain decode)
+    const void* k_new;          // [B, Hkv, D] dtype
+    const void* v_new;
+    const int64_t* new_slots;   // [B] slot of position seq_lens[s] - 1 (negative: nothing to write)
 };
 
 // Everything one pa_prefill call needs on the device.

@@ -7,8 +7,10 @@ cache", flow per step):
   1. host: reserve one position per sequence (copy-on-write pairs), slot of
      the new position, length + 1, padded block tables   (C++ manager)
   2. device: one pa_copy_blocks over every layer for all the step's pairs
-  3. device, per layer: one pa_kv_append of all the step's new K/V rows
-     (arrivals' prompts and one token per sequence), then pa_decode
+  3. device, per layer: the step's new K/V rows into the pool, then the
+     decode: pa_kv_append of the arrivals' prompt rows and one pa_decode_append
+     that writes each sequence's newest row and decodes (16-bit pools), or one
+     pa_kv_append of all the rows followed by pa_decode
 The host part of a step is planned separately (``plan_step``) from its device
 part (``run_step``) so that a benchmark can keep the plans of many steps
 resident on the device and time the device path alone.
@@ -62,10 +64,12 @@ class DeviceStep:
 
 
 class Replay:
-    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None, kv="native"):
+    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None, kv="native", fused=True):
         """kv = "native": pools in the workload's dtype; kv = "fp8": E4M3 pools
-        with the workload's per-(layer, KV head) scales."""
+        with the workload's per-(layer, KV head) scales.  fused: each layer's
+        newest rows go with its decode in one pa_decode_append (16-bit pools)."""
         self.wl = wl
+        self.fused = fused and kv == "native" and wl.dtype in ("f16", "bf16")
         self.device = torch.device(device)
         self.layers = list(range(wl.layers)) if layers is None else list(layers)
         self.host = HostBlockManager(wl.num_blocks, wl.b, wl.free_order)
@@ -104,6 +108,34 @@ class Replay:
         else:
             api.pa_decode(out, q, self.k_pools[li], self.v_pools[li], tables, lens, self.wl.scale,
                           partition_tokens=self.partition_tokens, workspace=ws, stream=stream)
+
+    def step_layer(self, li: int, out, q, k_new, v_new, slots, tables, lens, workspace, stream=None,
+                   events=None) -> int:
+        """One layer of a decode step: the step's rows into the pool, then the
+        decode.  k_new / v_new / slots hold the arrivals' prompt rows first, then
+        one row per sequence (its newest position); with `fused` those last B rows
+        go with the decode in one pa_decode_append.  `events` (a pair) brackets the
+        decode launch.  Returns the number of launches made (merge not counted)."""
+        B, T = q.shape[0], k_new.shape[0]
+        launches = 0
+        if not self.fused:
+            self.append(li, k_new, v_new, slots, stream=stream)
+            launches += 1
+        elif T > B:
+            self.append(li, k_new[:T - B], v_new[:T - B], slots[:T - B], stream=stream)
+            launches += 1
+        if events is not None:
+            events[0].record(stream if stream is not None else torch.cuda.current_stream())
+        if self.fused:
+            ws = workspace if workspace is not None and workspace.numel() else None
+            api.pa_decode_append(out, q, k_new[T - B:], v_new[T - B:], slots[T - B:], self.k_pools[li],
+                                 self.v_pools[li], tables, lens, self.wl.scale, partition_tokens=self.partition_tokens,
+                                 workspace=ws, stream=stream)
+        else:
+            self.decode(li, out, q, tables, lens, workspace, stream=stream)
+        if events is not None:
+            events[1].record(stream if stream is not None else torch.cuda.current_stream())
+        return launches + 1
 
     # ------------------------------------------------------------------ ops
     def _copy(self, pairs: np.ndarray):
@@ -188,10 +220,11 @@ class Replay:
     def device_step(self, plan: StepPlan) -> DeviceStep:
         """Upload the plan and generate the step's q and new K/V rows on the device.
 
-        Every row the step appends -- the prompts of arriving sequences and one
-        token per decoding sequence -- goes into one pa_kv_append per layer, and
-        every copy-on-write pair into one pa_copy_blocks (copies first: a
-        copy's source is a shared block, which no append of the step touches)."""
+        Every row the step appends -- the prompts of arriving sequences, then one
+        token per decoding sequence in batch order -- is generated per layer
+        (step_layer writes them), and every copy-on-write pair goes into one
+        pa_copy_blocks (copies first: a copy's source is a shared block, which no
+        append of the step touches)."""
         wl, dev = self.wl, self.device
         writes = plan.writes or []
         owners = np.array([wl.content_owner(u, int(p)) for u, p in zip(plan.uids, plan.positions)])
@@ -225,6 +258,6 @@ class Replay:
         if outs is None:
             outs = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
         for li in range(len(self.layers)):
-            self.append(li, ds.k_new[li], ds.v_new[li], ds.slots, stream=stream)
-            self.decode(li, outs[li], ds.q[li], ds.tables, ds.lens, ws, stream=stream)
+            self.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables, ds.lens, ws,
+                            stream=stream)
         return outs
