@@ -107,7 +107,7 @@ def _launch_key(args, wl, rp) -> str:
         key += f"+p{rp.partition_tokens}"
     if args.kernel != "auto":
         key += f"+{args.kernel}"
-    if not rp.fused:
+    if args.unfused and args.kv == "native":
         key += "+unfused"
     return key
 

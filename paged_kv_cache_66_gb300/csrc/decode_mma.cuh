@@ -110,10 +110,12 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// two E4M3 codes (low byte first) -> f16x2 (exact)
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// four E4M3 codes -> two f16x2 (exact): bytes 0, 1 -> lo (byte 0 in the low half), bytes 2, 3 -> hi
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l16;\n\tcvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
 }
 
 template <typename T>
@@ -353,12 +355,13 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                 if constexpr (F8) {
 #pragma unroll
                     for (int ks = 0; ks < KSTEPS; ks += 2) {
-                        uint32_t r[4];
+                        uint32_t r[4], a0[4], a1[4];
                         ldsm_x4(kbase + swz(lr + (lm & 1) * 8, ks + (lm >> 1)), r);
-                        const uint32_t a0[4] = {e4m3x2_to_h2(r[0]), e4m3x2_to_h2(r[1]), e4m3x2_to_h2(r[0] >> 16),
-                                                e4m3x2_to_h2(r[1] >> 16)};
-                        const uint32_t a1[4] = {e4m3x2_to_h2(r[2]), e4m3x2_to_h2(r[3]), e4m3x2_to_h2(r[2] >> 16),
-                                                e4m3x2_to_h2(r[3] >> 16)};
+                        // lane holds dims 4t..4t+3 of rows g and g+8: {r0 lo, r1 lo, r0 hi, r1 hi} per k-step
+                        e4m3x4_to_h2x2(r[0], a0[0], a0[2]);
+                        e4m3x4_to_h2x2(r[1], a0[1], a0[3]);
+                        e4m3x4_to_h2x2(r[2], a1[0], a1[2]);
+                        e4m3x4_to_h2x2(r[3], a1[1], a1[3]);
                         mma16816<TM>(sc, a0, qb[ks][0], qb[ks][1]);
                         mma16816<TM>(sc2, a1, qb[ks + 1][0], qb[ks + 1][1]);
                     }
@@ -425,17 +428,14 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                 if constexpr (F8) {
 #pragma unroll
                     for (int mt = 0; mt < KSTEPS; mt += 2) {
-                        uint32_t r[4];
+                        uint32_t r[4], a0[4], a1[4];
                         ldsm_x4_t(vbase + swz(lr + (lm & 1) * 8, mt + (lm >> 1)), r);
-                        // r[i] bytes: (tok 2t, dim 2g), (tok 2t, dim 2g+1), (tok 2t+1, dim 2g), (tok 2t+1, dim 2g+1)
-                        const uint32_t a0[4] = {e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x20u)),
-                                                e4m3x2_to_h2(__byte_perm(r[0], 0u, 0x31u)),
-                                                e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x20u)),
-                                                e4m3x2_to_h2(__byte_perm(r[1], 0u, 0x31u))};
-                        const uint32_t a1[4] = {e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x20u)),
-                                                e4m3x2_to_h2(__byte_perm(r[2], 0u, 0x31u)),
-                                                e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x20u)),
-                                                e4m3x2_to_h2(__byte_perm(r[3], 0u, 0x31u))};
+                        // r[i] bytes: (tok 2t, dim 2g), (tok 2t, dim 2g+1), (tok 2t+1, dim 2g), (tok 2t+1, dim 2g+1);
+                        // one byte permute groups each dim's two tokens: [b0 b2 | b1 b3]
+                        e4m3x4_to_h2x2(__byte_perm(r[0], 0u, 0x3120u), a0[0], a0[1]);
+                        e4m3x4_to_h2x2(__byte_perm(r[1], 0u, 0x3120u), a0[2], a0[3]);
+                        e4m3x4_to_h2x2(__byte_perm(r[2], 0u, 0x3120u), a1[0], a1[1]);
+                        e4m3x4_to_h2x2(__byte_perm(r[3], 0u, 0x3120u), a1[2], a1[3]);
                         mma16816<TM>(acc[mt], a0, pb0, pb1);
                         mma16816<TM>(acc[mt + 1], a1, pb0, pb1);
                     }
