@@ -310,63 +310,66 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
 
     if (warp == C::ISSUER) {
         // ------------------------------------------------------------ MMA issuer (one lane)
-        // S_Xj once K_j has landed and tile X's S buffer j % NSB has been consumed (j < jp_X + NSB);
-        // O_X += P_Xj V_j once the softmax of tile X has written P_Xj.  The four streams are
-        // polled so that none waits behind another.
+        // Fixed order, one K/V tile ahead: S_A(j+1) and S_B(j+1) back to back as soon as K_(j+1)
+        // has landed, then O_A += P_Aj V_j and O_B += P_Bj V_j as each softmax group delivers.
+        // The softmax of tile j then overlaps P.V of tile j-1 and the scores of tile j+1 on the
+        // tensor pipe.  S buffer (j+1) % NSB held P_(j-1), whose P.V was issued before (the
+        // pipe executes one thread's MMAs in order).
         if (lane == 0) {
             constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
             constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
             bool ok = mbar_wait_bounded(q_full, 0);
             tc05::fence_after();
-            int js[2] = {0, 0}, jp[2] = {0, 0};
-            uint64_t t_last = global_timer_ns();
-            while (ok && (jp[0] < n_kv || jp[1] < n_kv)) {
-                bool progressed = false;
+            auto issue_s = [&](int j) {
+                const uint32_t kb = sbase + C::KV_OFF + (j % STAGES) * C::STAGE_BYTES;
 #pragma unroll
                 for (int X = 0; X < 2; ++X) {
-                    const int j = js[X];
-                    // kv_full of tile j cannot move on before this S is issued (its refill needs both
-                    // tiles' P . V of tile j), so its phase parity is unambiguous here
-                    if (j < n_kv && j < jp[X] + NSB && tc05::test_wait(&kv_full[j % STAGES], (j / STAGES) & 1)) {
-                        tc05::fence_after();
-                        const uint32_t kb = sbase + C::KV_OFF + (j % STAGES) * C::STAGE_BYTES;
-                        const uint32_t qa = sbase + X * NBOX * C::QBOX;
-                        const uint32_t sd = tmem + C::S_COL + (X * NSB + j % NSB) * BN;
+                    const uint32_t qa = sbase + X * NBOX * C::QBOX;
+                    const uint32_t sd = tmem + C::S_COL + (X * NSB + j % NSB) * BN;
 #pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint64_t a = tc05::sdesc(qa + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
-                            const uint64_t b = tc05::sdesc(kb + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
-                            tc05::mma(sd, a, b, ID_S, ks > 0);
-                        }
-                        tc05::commit(&s_full[X * NSB + j % NSB]);
-                        ++js[X];
-                        progressed = true;
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t a = tc05::sdesc(qa + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
+                        const uint64_t b = tc05::sdesc(kb + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
+                        tc05::mma(sd, a, b, ID_S, ks > 0);
                     }
-                    const int t = jp[X];
-                    // P_X(t + NSB) needs S_X(t + NSB), which waits for this P . V: at most one phase ahead
-                    if (t < js[X] && tc05::test_wait(&p_full[X * NSB + t % NSB], (t / NSB) & 1)) {
-                        tc05::fence_after();
-                        const int st = t % STAGES;
-                        const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
-                        const uint32_t pa = tmem + C::S_COL + (X * NSB + t % NSB) * BN;  // key k at column k / 2
+                    tc05::commit(&s_full[X * NSB + j % NSB]);
+                }
+            };
+            // kv_full of tile j cannot complete another phase before kv_empty of tile j is
+            // committed (below, after both P.V of tile j), so each wait's parity is unambiguous
+            if (ok && n_kv > 0) {
+                ok = mbar_wait_bounded(&kv_full[0], 0);
+                if (ok) {
+                    tc05::fence_after();
+                    issue_s(0);
+                }
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (j + 1 < n_kv) {
+                    ok = mbar_wait_bounded(&kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1);
+                    if (!ok) break;
+                    tc05::fence_after();
+                    issue_s(j + 1);
+                }
+                const int st = j % STAGES;
+                const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            // N = D in one MMA: the 64-dim boxes of V are KV_BOX apart (leading byte offset)
-                            const uint64_t b = tc05::sdesc(vb + kk * 2048, C::KV_BOX, 1024);
-                            tc05::mma_ts(tmem + C::O_COL + X * D, pa + kk * 8, b, ID_PV, (t > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc05::commit(&o_ready[X]);
-                        // the stage is free once both tiles' P . V on it have completed
-                        if (jp[1 - X] > t) tc05::commit(&kv_empty[st]);
-                        ++jp[X];
-                        progressed = true;
+                for (int X = 0; X < 2; ++X) {
+                    // P_X(j + NSB) needs S_X(j + NSB), issued after this P.V: at most one phase ahead
+                    ok = mbar_wait_bounded(&p_full[X * NSB + j % NSB], (j / NSB) & 1);
+                    if (!ok) break;
+                    tc05::fence_after();
+                    const uint32_t pa = tmem + C::S_COL + (X * NSB + j % NSB) * BN;  // key k at column k / 2
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // N = D in one MMA: the 64-dim boxes of V are KV_BOX apart (leading byte offset)
+                        const uint64_t b = tc05::sdesc(vb + kk * 2048, C::KV_BOX, 1024);
+                        tc05::mma_ts(tmem + C::O_COL + X * D, pa + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
+                    tc05::commit(&o_ready[X]);
                 }
-                if (progressed) {
-                    t_last = global_timer_ns();
-                } else if (global_timer_ns() - t_last > 1000000000ull) {
-                    ok = false;
-                }
+                if (!ok) break;
+                tc05::commit(&kv_empty[st]);  // the stage is free once both tiles' P.V on it complete
             }
             if (ok) tc05::commit(o_final);
             else flag_error(p.err, PA_DEVERR_TIMEOUT);
