@@ -320,16 +320,22 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
             constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
             bool ok = mbar_wait_bounded(q_full, 0);
             tc05::fence_after();
+            // Descriptors are formed once; an operand at byte offset o from a base has the base's
+            // descriptor plus o / 16 (shared addresses stay below 2^18, so the 14-bit start field
+            // never carries).  This keeps the issuing thread's instructions per MMA few: it shares
+            // its scheduler with two softmax warps.
+            const uint64_t q_desc = tc05::sdesc(sbase, 16, 1024);
+            const uint64_t k_desc = tc05::sdesc(sbase + C::KV_OFF, 16, 1024);
+            const uint64_t v_desc = tc05::sdesc(sbase + C::KV_OFF + C::K_BYTES, C::KV_BOX, 1024);
             auto issue_s = [&](int j) {
-                const uint32_t kb = sbase + C::KV_OFF + (j % STAGES) * C::STAGE_BYTES;
+                const uint64_t kst = k_desc + static_cast<uint64_t>((j % STAGES) * (C::STAGE_BYTES >> 4));
 #pragma unroll
                 for (int X = 0; X < 2; ++X) {
-                    const uint32_t qa = sbase + X * NBOX * C::QBOX;
                     const uint32_t sd = tmem + C::S_COL + (X * NSB + j % NSB) * BN;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t a = tc05::sdesc(qa + (ks >> 2) * C::QBOX + (ks & 3) * 32, 16, 1024);
-                        const uint64_t b = tc05::sdesc(kb + (ks >> 2) * C::KV_BOX + (ks & 3) * 32, 16, 1024);
+                        const uint64_t a = q_desc + static_cast<uint64_t>((X * NBOX * C::QBOX + (ks >> 2) * C::QBOX + (ks & 3) * 32) >> 4);
+                        const uint64_t b = kst + static_cast<uint64_t>(((ks >> 2) * C::KV_BOX + (ks & 3) * 32) >> 4);
                         tc05::mma(sd, a, b, ID_S, ks > 0);
                     }
                     tc05::commit(&s_full[X * NSB + j % NSB]);
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
                     issue_s(j + 1);
                 }
                 const int st = j % STAGES;
-                const uint32_t vb = sbase + C::KV_OFF + st * C::STAGE_BYTES + C::K_BYTES;
+                const uint64_t vst = v_desc + static_cast<uint64_t>(st * (C::STAGE_BYTES >> 4));
 #pragma unroll
                 for (int X = 0; X < 2; ++X) {
                     // P_X(j + NSB) needs S_X(j + NSB), issued after this P.V: at most one phase ahead
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(Tc05Cfg<D>::THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         // N = D in one MMA: the 64-dim boxes of V are KV_BOX apart (leading byte offset)
-                        const uint64_t b = tc05::sdesc(vb + kk * 2048, C::KV_BOX, 1024);
+                        const uint64_t b = vst + static_cast<uint64_t>((kk * 2048) >> 4);
                         tc05::mma_ts(tmem + C::O_COL + X * D, pa + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc05::commit(&o_ready[X]);
