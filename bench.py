@@ -600,7 +600,7 @@ def main():
     ap.add_argument("--partition", type=int, default=0, help="decode partition tokens (0: the workload's)")
     ap.add_argument("--copy-layers", type=int, default=32, help="--op copy: layers (pools of 4096 blocks each)")
     ap.add_argument("--copy-pairs", type=int, default=64, help="--op copy: copy-on-write pairs")
-    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc05"], help="--op prefill kernel")
+    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc05", "tc05w"], help="--op prefill kernel")
     ap.add_argument("--prefill-dtype", default="bf16", choices=["f16", "bf16"], help="--op prefill storage dtype")
     ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host", "prefill"],
                     help="step = the benchmark line; others measure one row of the path alone")

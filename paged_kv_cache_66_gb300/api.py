@@ -231,11 +231,12 @@ def pa_set_decode_kernel(kernel: str) -> None:
     check(load().pa_set_decode_kernel(DECODE_KERNELS[kernel]), "pa_set_decode_kernel")
 
 
-PREFILL_KERNELS = {"auto": 0, "mma": 1, "tc05": 2}
+PREFILL_KERNELS = {"auto": 0, "mma": 1, "tc05": 2, "tc05w": 3}
 
 
 def pa_set_prefill_kernel(kernel: str) -> None:
-    """Process-wide pa_prefill kernel: "auto" (tcgen05 where it applies), "mma" or "tc05"."""
+    """Process-wide pa_prefill kernel: "auto" (tcgen05 where it applies), "mma", "tc05" (64-key
+    tiles) or "tc05w" (128-key tiles, D = 128)."""
     check(load().pa_set_prefill_kernel(PREFILL_KERNELS[kernel]), "pa_set_prefill_kernel")
 
 

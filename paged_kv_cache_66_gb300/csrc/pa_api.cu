@@ -114,7 +114,9 @@ pa_status pa_set_decode_kernel(pa_decode_kernel kernel) {
 }
 
 pa_status pa_set_prefill_kernel(pa_prefill_kernel kernel) {
-    if (kernel != PA_PREFILL_AUTO && kernel != PA_PREFILL_MMA && kernel != PA_PREFILL_TC05) return PA_ERR_INVALID;
+    if (kernel != PA_PREFILL_AUTO && kernel != PA_PREFILL_MMA && kernel != PA_PREFILL_TC05 &&
+        kernel != PA_PREFILL_TC05W)
+        return PA_ERR_INVALID;
     g_prefill_kernel.store(kernel);
     return PA_OK;
 }

@@ -1,20 +1,27 @@
 // Choice between the prefill kernels for one pa_prefill call: the tcgen05
-// kernel (prefill_tc05.cuh) for D in {64, 128} unless the caller forced the
-// warp-level one (prefill_mma.cuh), which covers every D.
+// kernels for D in {64, 128} (128-key tiles, prefill_tc05w.cuh, at D = 128;
+// 64-key tiles, prefill_tc05.cuh, at D = 64 or when forced) unless the caller
+// forced the warp-level one (prefill_mma.cuh), which covers every D.
 #pragma once
 
 #include "prefill_mma.cuh"
 #include "prefill_tc05.cuh"
+#include "prefill_tc05w.cuh"
 
 namespace pa {
 
 template <typename T, int D, int G>
 cudaError_t launch_prefill_path(const PrefillParams& p, const CUtensorMap& km, const CUtensorMap& vm, int max_q,
                                 cudaStream_t stream) {
+    if constexpr (D == 128) {
+        if (p.kernel == PA_PREFILL_TC05W || p.kernel == PA_PREFILL_AUTO)
+            return launch_prefill_tc05w<T, G>(p, km, vm, max_q, stream);
+    }
     if constexpr (D <= 128) {
+        if (p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
         if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05<T, D, G>(p, km, vm, max_q, stream);
     } else {
-        if (p.kernel == PA_PREFILL_TC05) return cudaErrorNotSupported;
+        if (p.kernel == PA_PREFILL_TC05 || p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
     }
     return launch_prefill<T, D, G>(p, km, vm, max_q, stream);
 }

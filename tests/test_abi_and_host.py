@@ -93,6 +93,20 @@ def test_workspace_size():
     assert lib.pa_decode_workspace_size(8, 32, 128, 2048, 16, 0) == ml + rows * 128 * 4
 
 
+def test_kernel_choices_accept_the_declared_values_only():
+    """pa_set_decode_kernel / pa_set_prefill_kernel store a process-wide choice
+    (host only): the enum values of include/pagedkv.h are taken, others refused."""
+    lib = _lib.load()
+    for k in (0, 1, 2, 3):
+        assert lib.pa_set_prefill_kernel(k) == 0
+    assert lib.pa_set_prefill_kernel(4) == 1                # PA_ERR_INVALID
+    assert lib.pa_set_prefill_kernel(-1) == 1
+    for k in (0, 1, 2):
+        assert lib.pa_set_decode_kernel(k) == 0
+    assert lib.pa_set_decode_kernel(3) == 1
+    assert lib.pa_set_prefill_kernel(0) == 0 and lib.pa_set_decode_kernel(0) == 0
+
+
 # ------------------------------------------------------------------ host manager
 
 def test_host_slot_example_and_exceptions():

@@ -93,10 +93,12 @@ CASES = [
     (4, 4, 64, 256, [600], [600]),                      # b = 256, G = 1: 600 chunk rows over 3 CTAs
     (4, 4, 128, 16, [700], [700]),                      # G = 1, a whole 256-row CTA plus a ragged one
     (6, 3, 128, 16, [200, 90], [100, 90]),              # odd Hkv
+    (16, 2, 128, 16, [1500, 777], [300, 777]),          # G = 8: many 128-key tiles, ragged ends
+    (8, 2, 128, 256, [900], [400]),                     # b = 256 at D = 128
 ]
 
 
-@pytest.fixture(params=["mma", "tc05"])
+@pytest.fixture(params=["mma", "tc05", "tc05w"])
 def kernel(request, api):
     api.pa_set_prefill_kernel(request.param)
     yield request.param
@@ -107,7 +109,7 @@ def kernel(request, api):
 @pytest.mark.parametrize("case", CASES)
 def test_prefill_matches_oracle(api, kernel, dtype, case):
     Hq, Hkv, D, b, lengths, chunks = case
-    if kernel == "tc05" and D == 256:
+    if (kernel == "tc05" and D == 256) or (kernel == "tc05w" and D != 128):
         K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype, seed=1)
         with pytest.raises(api.PagedKVError) as e:
             _run(api, K, V, q, tables, lens, qstart, 0.1)
@@ -139,7 +141,7 @@ def test_prefill_chunk_of_one_equals_decode(api, kernel):
 
 
 def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api, kernel):
-    Hq, Hkv, D, b = 8, 2, 64, 16
+    Hq, Hkv, D, b = 8, 2, (128 if kernel == "tc05w" else 64), 16
     K, V, q, tables, lens, qstart = _setup([20, 30], [5, 6], Hq, Hkv, D, b, torch.float16, seed=11)
     lens[0] = 3                                           # chunk of 5 > length 3
     got = _run(api, K, V, q, tables, lens, qstart, 0.125)
@@ -151,7 +153,7 @@ def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api, kernel):
 
 
 def test_prefill_bad_table_entry_is_flagged(api, kernel):
-    Hq, Hkv, D, b = 8, 2, 64, 16
+    Hq, Hkv, D, b = 8, 2, (128 if kernel == "tc05w" else 64), 16
     K, V, q, tables, lens, qstart = _setup([40], [40], Hq, Hkv, D, b, torch.float16, seed=12)
     tables[0, 1] = K.shape[0] + 7
     _run(api, K, V, q, tables, lens, qstart, 0.125)
