@@ -17,8 +17,9 @@
 // K and V slots (two of each, 32 KiB per 128-key tile) are released separately:
 // K_j once both S_j have completed, V_j once both P . V_j have, each refilled by
 // its own producer warp; every slot then has about two iterations to land.
-// Warps: 0-7 softmax (group X = warp / 4, thread = row), 8 K producer, 9 MMA
-// issuer, 10 V producer.  Every wait is bounded (1 s), each barrier a waiter may
+// Warps: 0-15 softmax (group X = warp / 8; two threads per row, one per 64-key
+// half, meeting once per tile to combine the row max), 16 K producer, 17 MMA
+// issuer, 18 V producer.  Every wait is bounded (1 s), each barrier a waiter may
 // skip phases of is at most one phase ahead of it (comments at each wait), and
 // every warp-collective tcgen05 load / store sits behind warp-uniform decisions.
 #pragma once
@@ -41,11 +42,12 @@ struct Tc05wCfg {
     // k_full, k_empty, v_full, v_empty [SLOTS]; s_full, p_full [2]; o_final; q_full
     static constexpr int NBARS = 4 * SLOTS + 4 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr size_t smem_bytes = 1024 + MISC_OFF + 16 + 4 * SLOTS;
+    static constexpr int RED_OFF = MISC_OFF + 64;  // row max exchange [2][2][2][128], row sums [2][2][128]
+    static constexpr size_t smem_bytes = 1024 + RED_OFF + (8 + 4) * 128 * 4;
     // tensor memory: O_A [0, 128), O_B [128, 256), S_A [256, 384), S_B [384, 512)
     static constexpr int O_COL = 0, S_COL = 2 * D;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NSW = 8;
+    static constexpr int NSW = 16;  // two groups of eight: two threads (key halves) per row
     static constexpr int PRODUCER_K = NSW, ISSUER = NSW + 1, PRODUCER_V = NSW + 2;
     static constexpr int THREADS = (NSW + 3) * 32;
     static constexpr int SUB = BN / 16;  // 16-key sub-tiles (one block row each) per tile
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
 #pragma unroll
         for (int X = 0; X < 2; ++X) {
             mbar_init(&s_full[X], 1);
-            mbar_init(&p_full[X], 128);
+            mbar_init(&p_full[X], 256);
         }
         mbar_init(o_final, 1);
         mbar_init(q_full, C::NSW * 32);
@@ -250,9 +252,12 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
         return;
     }
 
-    // ------------------------------------------------------------ softmax warps (thread = row)
-    const int X = warp >> 2, r = tid & 127;  // query tile, row within it
-    const int wq = warp & 3;
+    // ------------------------------------------------------------ softmax warps (two threads per row)
+    // warp w: tile X = w / 8, key half hh = (w / 4) % 2 (columns 64 hh .. 64 hh + 63 of S, 32 hh ..
+    // of P, dims 64 hh .. of O), rows 32 (w % 4) .. +31 = its TMEM lanes; warps w and w + 4 share
+    // their rows and meet once per tile to combine the row max
+    const int X = warp >> 3, hh = (warp >> 2) & 1, wq = warp & 3;
+    const int r = wq * 32 + lane;     // row within tile X
     const int prow_id = X * 128 + r;  // packed row of the CTA
     const int tok = tok0 + prow_id / G;
     const bool valid = tok < Cq;
@@ -262,73 +267,87 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
     const int warp_tok = tok0 + (X * 128 + wq * 32) / G;
     const int warp_pos_min = warp_tok < Cq ? base + warp_tok : -1;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t o_addr = lane_addr + C::O_COL + X * D;
+    const uint32_t o_addr = lane_addr + C::O_COL + X * D + hh * 64;
     const uint32_t sa = lane_addr + C::S_COL + X * BN;
+    float* xmax = reinterpret_cast<float*>(smem + C::RED_OFF);  // [tile parity][X][half][row]
+    float* xl = xmax + 2 * 2 * 2 * 128;                          // [X][half][row]
+    const int gbar = 3 + X;                                      // the group's named barrier (256 threads)
     {
-        // Q row into tile X's K-major swizzled operand (zeros past the chunk)
+        // this half of the Q row into tile X's K-major swizzled operand (zeros past the chunk)
         const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                           (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D);
-        unsigned char* qx = smem + X * NBOX * C::QBOX;
+                                                           (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D) +
+                            hh * 8;
+        unsigned char* qx = smem + X * NBOX * C::QBOX + hh * C::QBOX;
 #pragma unroll
-        for (int cc = 0; cc < D / 8; ++cc) {
-            const int bx = cc >> 3, c = cc & 7;
-            const uint4 v = valid ? __ldg(qrow + cc) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(qx + bx * C::QBOX + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(qx + r * 128 + ((c ^ (r & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
         mbar_arrive(q_full);
     }
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
         const int sl = j % SLOTS;
         // decisions that guard a tcgen05.ld / st are warp-uniform (those are .sync.aligned).
         // Neither barrier can run two phases ahead: V of tile j + SLOTS is loaded, and S_X(j + 1)
         // issued, only after this thread's P_Xj has been consumed
-        const bool got = mbar_wait_bounded(&v_full[sl], (j / SLOTS) & 1) && mbar_wait_bounded(&s_full[X], j & 1);
-        if (!__all_sync(0xffffffffu, got)) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&v_full[sl], (j / SLOTS) & 1) &&
+                                                     mbar_wait_bounded(&s_full[X], j & 1));
+        const int key0 = j * BN;
+        int okmask = 0;
+        bool interior = false;
+        uint32_t sr[64];
+        float pmx = -INFINITY;
+        if (got) {
+            tc05::fence_after();
+            okmask = slot_ok[sl];
+            // interior tile: every valid row of the warp sees all 128 keys and the scale is positive
+            interior = okmask == (1 << SUB) - 1 && key0 + BN - 1 <= warp_pos_min && sl2 > 0.f;
+            // this half's 64 scores in registers; masked tiles are scaled and masked in place
+            // (invisible keys: -inf), so the exponentials below are branch-free
+            tc05::ld32(sa + hh * 64, sr);
+            tc05::ld32(sa + hh * 64 + 32, sr + 32);
+            tc05::wait_ld();
+            float t[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t[i] = -INFINITY;
+            if (interior) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) t[c & 7] = fmaxf(t[c & 7], __uint_as_float(sr[c]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int key = hh * 64 + c;
+                    const bool vis = key0 + key <= pos && ((okmask >> (key >> 4)) & 1);
+                    const float x = vis ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+                    sr[c] = __float_as_uint(x);
+                    t[c & 7] = fmaxf(t[c & 7], x);
+                }
+            }
+            pmx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
+            if (interior) pmx *= sl2;
+            xmax[(((j & 1) * 2 + X) * 2 + hh) * 128 + r] = pmx;
+        }
+        // every thread of the group arrives here once per tile, so a timeout ends the loop for the
+        // whole group at the same tile; the partner's max of tile j sits in the parity-j buffer,
+        // which is written again (tile j + 2) only after both have passed tile j + 1's barrier
+        if (!tc05::bar_and(gbar, 256, got)) {
             ok = false;
             break;
         }
-        tc05::fence_after();
-        const int key0 = j * BN;
-        const int okmask = slot_ok[sl];
-        // interior tile: every valid row of the warp sees all 128 keys and the scale is positive
-        const bool interior = okmask == (1 << SUB) - 1 && key0 + BN - 1 <= warp_pos_min && sl2 > 0.f;
-        // ---- the row's 128 scores in registers (one wait for all four loads); masked tiles are
-        // scaled and masked in place (invisible keys: -inf), so the exponentials below are
-        // branch-free: P = 2^(v * mul - m) with mul = scale (interior, raw scores) or 1
-        uint32_t sr[128];
-#pragma unroll
-        for (int c = 0; c < 128; c += 32) tc05::ld32(sa + c, sr + c);
-        tc05::wait_ld();
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = -INFINITY;
-        if (interior) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) t[c & 7] = fmaxf(t[c & 7], __uint_as_float(sr[c]));
-        } else {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const bool vis = key0 + c <= pos && ((okmask >> (c >> 4)) & 1);
-                const float x = vis ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-                sr[c] = __float_as_uint(x);
-                t[c & 7] = fmaxf(t[c & 7], x);
-            }
-        }
-        float mx = fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
-        if (interior) mx *= sl2;
-        // lazy rescale per row; O_X is rescaled for the whole warp when any row needs it, each lane
-        // by its own factor.  No P . V of tile X is in flight: S_X(j) was issued after
+        const float mx = fmaxf(pmx, xmax[(((j & 1) * 2 + X) * 2 + (hh ^ 1)) * 128 + r]);
+        // lazy rescale per row (both threads of a row decide alike); O_X is rescaled for the whole
+        // warp when any row needs it.  No P . V of tile X is in flight: S_X(j) was issued after
         // P_X(j-1) . V_(j-1), and its completion, seen above, reports that one's too
         const bool grow = mx > m + kLazyRescale;
         const bool scale_o = grow && m != -INFINITY;
         const float a = scale_o ? tc05::fast_exp2(m - mx) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t o[32];
                 tc05::ld32(o_addr + c0, o);
                 tc05::wait_ld();
@@ -343,11 +362,11 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
         }
         const float ms = m == -INFINITY ? 0.f : m;
         const float mul = interior ? sl2 : 1.f;
-        // ---- P = 2^(v * mul - m): keys 32q .. 32q+31 go to columns 16q .. 16q+15 (two 16-bit
-        // values per column), over scores already in registers
+        // ---- P = 2^(v * mul - m): keys 64 hh + 32 q .. +31 go to columns 32 hh + 16 q .. +15
+        // (two 16-bit values per column), over scores already in registers
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
+        for (int qq = 0; qq < 2; ++qq) {
             uint32_t pw[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -357,14 +376,14 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
                 ls[i & 3] += e0 + e1;
                 pw[i] = pack2<T>(e0, e1);
             }
-            tc05::st16(sa + qq * 16, pw);
+            tc05::st16(sa + hh * 32 + qq * 16, pw);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero them
         // (both groups write the same zeros; each P . V waits only for its own group's)
         if (key0 + BN > L || okmask != (1 << SUB) - 1) {
             unsigned char* vt = smem + C::V_OFF + sl * C::SLOT_BYTES;
-            for (int e = r; e < BN * NBOX * 8; e += 128) {
+            for (int e = hh * 128 + r; e < BN * NBOX * 8; e += 256) {
                 const int key = e / (NBOX * 8), rest = e % (NBOX * 8);
                 if (key0 + key >= L || !((okmask >> (key >> 4)) & 1))
                     *reinterpret_cast<uint4*>(vt + (rest >> 3) * C::KV_BOX + key * 128 + (rest & 7) * 16) =
@@ -379,12 +398,17 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
     griddep_launch_dependents();
     const bool all_ok = tc05::bar_and(2, C::NSW * 32, ok);
     const bool done = all_ok && mbar_wait_bounded(o_final, 0);
+    // the row sum: this half's share plus the partner's (every softmax thread passed the barrier
+    // above, so the exchange below is reached by the whole group)
+    xl[(X * 2 + hh) * 128 + r] = l;
+    tc05::named_sync(gbar, 256);
+    const float lt = l + xl[(X * 2 + (hh ^ 1)) * 128 + r];
     if (__all_sync(0xffffffffu, done)) {
         tc05::fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + hh * 64;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t o[32];
             tc05::ld32(o_addr + c0, o);
             tc05::wait_ld();
