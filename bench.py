@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -191,6 +192,31 @@ def _kv_bytes(wl, lens, elt=None) -> int:
     return int(np.sum(np.asarray(lens, dtype=np.int64))) * 2 * wl.Hkv * wl.D * (wl.elt if elt is None else elt)
 
 
+def _unique_kv_bytes(wl, plan, elt=None) -> int:
+    """Unique K/V bytes one decode touches: distinct pool blocks in the batch's tables (a block
+    shared by many sequences counted once) x 2 * Hkv * b * D * (stored element size)."""
+    blocks = set()
+    for row, L in zip(np.asarray(plan.tables), np.asarray(plan.lens, dtype=np.int64)):
+        blocks.update(int(x) for x in row[: (int(L) + wl.b - 1) // wl.b])
+    return len(blocks) * 2 * wl.Hkv * wl.b * wl.D * (wl.elt if elt is None else elt)
+
+
+def _cpu_model() -> str:
+    """CPU model name from /proc/cpuinfo (x86 'model name'; Arm implementer / part), else the machine."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    m = re.search(r"^model name\s*:\s*(.+)$", info, flags=re.M)
+    if m:
+        return m.group(1).strip()
+    impl = re.search(r"^CPU implementer\s*:\s*(\S+)", info, flags=re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", info, flags=re.M)
+    if impl and part:
+        return f"{platform.machine()} implementer {impl.group(1)} part {part.group(1)}"
+    return platform.machine()
+
+
 def _alg_bytes_decode(wl, plan, kv_elt=None, fused=False) -> int:
     """Algorithmic bytes of one pa_decode launch: K/V history + q + out + block
     tables + lengths (scratch traffic of the split is not algorithmic).  A fused
@@ -238,7 +264,7 @@ def run_reference(args, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "sample": "one sequence of layer 0 per step"},
-            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": _cpu_model(),
                              "sample": f"one {wl.name} sequence x layer 0 per step, {args.steps} steps"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -272,6 +298,7 @@ def cpu_baseline(wl, budget_s: float = 15.0):
         n += 1
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": n * _kv_bytes(wl, [L]) / tt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": _cpu_model(),
             "sample": f"{n} decodes of one {L}-token sequence, layer 0 of {wl.name} (setup {time.perf_counter()-t0-tt:.1f}s untimed)"}
 
 
@@ -335,6 +362,9 @@ def run_ours(args, ws, rank, local):
     seq_steps = B * args.steps * ws / (dev_ms_max / 1e3)
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
     dec_avg = sum(dec_ms) / len(dec_ms)
+    dec_med = statistics.median(dec_ms)
+    unique = statistics.mean(_unique_kv_bytes(wl, dsteps[args.warmup + j].plan, rp.kv_elt) for j in range(args.steps))
+    effective = statistics.mean(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens, rp.kv_elt) for j in range(args.steps))
     alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan, rp.kv_elt, rp.fused)
                           for j in range(args.steps))
     peak, peak_kind = _peaks()
@@ -357,13 +387,15 @@ def run_ours(args, ws, rank, local):
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{ws}"},
         "seq_steps_per_s": seq_steps,
+        "kv_bytes_per_decode": {"effective": effective, "unique": unique,
+                                "unique_gbs_per_launch": unique / (dec_avg / 1e3) / 1e9},
         "pct_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(_launch_key(args, wl, rp)),
                      "kernel": (f"pa_decode_append ({args.kernel} partition with the step's append + merge)"
                                 if rp.fused else f"pa_decode ({args.kernel} partition + merge)"),
                      "peak_kind": f"{peak_kind} hbm_gbs",
-                     "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg},
+                     "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg, "median_launch_ms": dec_med},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
         "e2e": e2e,
