@@ -27,6 +27,32 @@
 #include "prefill_tc05.cuh"
 
 namespace pa {
+namespace tc05 {
+
+// max of three (one instruction on sm_100+)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// (y0, y1) = (x0 * m + b, x1 * m + b), one packed fp32 FMA (each lane rounded once, as fmaf)
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float m, float b) {
+    asm("{\n\t.reg .b64 x, mm, bb, y;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 mm, {%4, %4};\n\t"
+        "mov.b64 bb, {%5, %5};\n\tfma.rn.f32x2 y, x, mm, bb;\n\tmov.b64 {%0, %1}, y;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(x0), "f"(x1), "f"(m), "f"(b));
+}
+
+// (s0, s1) += (a0, a1), one packed fp32 add
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 s, a;\n\tmov.b64 s, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\t"
+        "add.rn.f32x2 s, s, a;\n\tmov.b64 {%0, %1}, s;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
+
+}  // namespace tc05
 
 struct Tc05wCfg {
     static constexpr int D = 128, BM = 256, BN = 128;
@@ -316,7 +342,8 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
             for (int i = 0; i < 8; ++i) t[i] = -INFINITY;
             if (interior) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) t[c & 7] = fmaxf(t[c & 7], __uint_as_float(sr[c]));
+                for (int c = 0; c < 64; c += 2)
+                    t[(c >> 1) & 7] = tc05::max3(t[(c >> 1) & 7], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
             } else {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
@@ -364,6 +391,7 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
         const float mul = interior ? sl2 : 1.f;
         // ---- P = 2^(v * mul - m): keys 64 hh + 32 q .. +31 go to columns 32 hh + 16 q .. +15
         // (two 16-bit values per column), over scores already in registers
+        // (pairs of keys in packed fp32 FMAs and adds: the softmax is issue-bound here)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
@@ -371,9 +399,10 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int c = qq * 32 + 2 * i;
-                const float e0 = tc05::fast_exp2(fmaf(__uint_as_float(sr[c]), mul, -ms));
-                const float e1 = tc05::fast_exp2(fmaf(__uint_as_float(sr[c + 1]), mul, -ms));
-                ls[i & 3] += e0 + e1;
+                float x0, x1;
+                tc05::fma2(x0, x1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), mul, -ms);
+                const float e0 = tc05::fast_exp2(x0), e1 = tc05::fast_exp2(x1);
+                tc05::add2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], e0, e1);
                 pw[i] = pack2<T>(e0, e1);
             }
             tc05::st16(sa + hh * 32 + qq * 16, pw);
