@@ -21,9 +21,11 @@
 //   O_X += P_Xj . V_j    tcgen05.mma M=128 N=D, A = P_Xj (tensor memory), B = V_j (smem,
 //                        MN-major: keys are the K dimension).
 // Warps: 0-7 softmax (warp w: tile w / 4, rows 32 (w % 4) .. +31 = its TMEM lanes),
-// 8 producer (TMA, four lanes issuing), 9 MMA issuer (one lane, polling the four
-// streams S_A, S_B, P_A, P_B with mbarrier.test_wait and issuing whichever is ready;
-// a K/V stage is released once both tiles' P . V on it have been issued).
+// 8 producer (TMA, four lanes issuing), 9 MMA issuer (one lane, fixed order one
+// K/V tile ahead: S_A(j+1) and S_B(j+1), then P_A(j) . V_j and P_B(j) . V_j; a
+// K/V stage is released once both tiles' P . V on it have completed).  The
+// 128-key kernel (prefill_tc05w.cuh) is the default at D = 128; this one serves
+// D = 64 and D = 128 when forced.
 // Hand-offs are mbarriers: TMA bytes (kv_full), MMA completion through
 // tcgen05.commit (s_full, o_ready per tile, o_final, kv_empty), softmax arrivals
 // (p_full).  Every wait is bounded (1 s of %globaltimer, PA_DEVERR_TIMEOUT), and no
