@@ -312,6 +312,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     api.pa_set_decode_kernel(args.kernel)
+    api.pa_set_decode_heads_per_cta(args.heads_per_cta)
     total_steps = args.warmup + args.steps
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
@@ -333,10 +334,13 @@ def run_ours(args, ws, rank, local):
     _barrier(ws)
 
     nL = len(rp.layers)
-    # per-launch events on the layers of the last timed step only: an event recorded between two
-    # launches ends their programmatic overlap, which cost ~2.5 % of the step when every launch
-    # was bracketed
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
+    # per-launch events on the launches of the last timed steps only (32 launches, or the last
+    # quarter of the steps when fewer): an event recorded between two launches ends their
+    # programmatic overlap, which cost ~2.5 % of the long-context step when every launch was
+    # bracketed, and ~30 % of the one-layer, L2-resident step
+    ev_steps = min(max(1, -(-32 // nL)), max(1, args.steps // 4))
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(ev_steps * nL)]
     clocks = ClockSampler(local)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
@@ -350,7 +354,9 @@ def run_ours(args, ws, rank, local):
             launches += 1
         for li in range(nL):
             launches += rp.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables,
-                                      ds.lens, wsbuf, events=ev_dec[li] if j == args.steps - 1 else None)
+                                      ds.lens, wsbuf,
+                                      events=ev_dec[(j - (args.steps - ev_steps)) * nL + li]
+                                      if j >= args.steps - ev_steps else None)
             launches += 1 if wsbuf.numel() else 0
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -368,7 +374,8 @@ def run_ours(args, ws, rank, local):
     dec_med = statistics.median(dec_ms)
     unique = statistics.mean(_unique_kv_bytes(wl, dsteps[args.warmup + j].plan, rp.kv_elt) for j in range(args.steps))
     effective = statistics.mean(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens, rp.kv_elt) for j in range(args.steps))
-    alg = _alg_bytes_decode(wl, dsteps[args.warmup + args.steps - 1].plan, rp.kv_elt, rp.fused)
+    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan, rp.kv_elt, rp.fused)
+                          for j in range(args.steps - ev_steps, args.steps))
     peak, peak_kind = _peaks()
     achieved = alg / (dec_avg / 1e3) / 1e9
     err = api.pa_get_device_error()
@@ -628,6 +635,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
+    ap.add_argument("--heads-per-cta", type=int, default=0, choices=[0, 1, 2],
+                    help="tensor-core decode: KV heads per CTA (0: chosen per launch)")
     ap.add_argument("--unfused", action="store_true",
                     help="decode step: separate append and decode launches instead of pa_decode_append")
     ap.add_argument("--kv", default="native", choices=["native", "fp8"], help="KV cache storage (fp8 = E4M3)")

@@ -294,6 +294,16 @@ typedef enum pa_decode_kernel {
 pa_status pa_set_decode_kernel(pa_decode_kernel kernel);
 
 /*
+ * pa_set_decode_heads_per_cta -- process-wide choice of how many KV heads one
+ * CTA of the tensor-core decode kernel streams back to back (its block-table
+ * slice staged once): 0 (default) takes two when that costs no resident CTA
+ * per SM (by the occupancy calculator), else one; 1 or 2 force it.  Results
+ * are identical either way.
+ * Returns PA_ERR_INVALID for any other value.
+ */
+pa_status pa_set_decode_heads_per_cta(int heads);
+
+/*
  * pa_set_prefill_kernel -- process-wide choice of the pa_prefill kernel (both
  * compute the same result within the attention tolerance):
  *   PA_PREFILL_AUTO  (default) PA_PREFILL_TC05W for D = 128, PA_PREFILL_TC05

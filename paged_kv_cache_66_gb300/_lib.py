@@ -38,6 +38,7 @@ SIGNATURES = {
     "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                           _f32, _i32, _vp]),
     "pa_set_decode_kernel": (_i32, [_i32]),
+    "pa_set_decode_heads_per_cta": (_i32, [_i32]),
     "pa_set_prefill_kernel": (_i32, [_i32]),
     "pa_selftest_wait_timeout": (_i32, [_i32, _vp]),
     "pa_get_device_error": (_i32, [C.POINTER(C.c_int), _vp]),

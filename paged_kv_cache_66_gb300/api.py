@@ -234,6 +234,11 @@ def pa_set_decode_kernel(kernel: str) -> None:
 PREFILL_KERNELS = {"auto": 0, "mma": 1, "tc05": 2, "tc05w": 3}
 
 
+def pa_set_decode_heads_per_cta(heads: int) -> None:
+    """KV heads per CTA of the tensor-core decode kernel: 0 (choose per launch), 1 or 2."""
+    check(load().pa_set_decode_heads_per_cta(int(heads)), "pa_set_decode_heads_per_cta")
+
+
 def pa_set_prefill_kernel(kernel: str) -> None:
     """Process-wide pa_prefill kernel: "auto" (tcgen05 where it applies), "mma", "tc05" (64-key
     tiles) or "tc05w" (128-key tiles, D = 128)."""

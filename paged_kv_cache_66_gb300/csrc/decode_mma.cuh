@@ -558,13 +558,16 @@ cudaError_t launch_mma(const DecodeParams& p_in, const CUtensorMap& kmap, const 
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, decode_partition_mma<T, PE, D, G>, C::NW * 32,
                                                               C::smem_bytes(entries, 2));
         if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
         cached_hpc = occ2 >= occ1 ? 2 : 1;
         cached_entries = entries;
     }
 #ifdef PA_MMA_HEADS
     p.heads_per_cta = PA_MMA_HEADS;  // build-time override (tuning sweeps)
 #else
-    p.heads_per_cta = p.hkv >= 2 ? cached_hpc : 1;
+    // two heads per CTA when it costs no resident CTA per SM, unless the caller forced 1 or 2
+    if (p.heads_per_cta != 1 && p.heads_per_cta != 2) p.heads_per_cta = cached_hpc;
+    if (p.hkv < 2) p.heads_per_cta = 1;
 #endif
     const size_t smem = C::smem_bytes(entries, p.heads_per_cta);
     dim3 grid(p.max_partitions, (p.hkv + p.heads_per_cta - 1) / p.heads_per_cta, p.batch);

@@ -36,6 +36,7 @@ int* error_word() {
 }
 
 std::atomic<int> g_decode_kernel{PA_DECODE_AUTO};
+std::atomic<int> g_decode_heads{0};
 std::atomic<int> g_prefill_kernel{PA_PREFILL_AUTO};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -110,6 +111,12 @@ extern "C" {
 pa_status pa_set_decode_kernel(pa_decode_kernel kernel) {
     if (kernel != PA_DECODE_AUTO && kernel != PA_DECODE_SIMT && kernel != PA_DECODE_MMA) return PA_ERR_INVALID;
     g_decode_kernel.store(kernel);
+    return PA_OK;
+}
+
+pa_status pa_set_decode_heads_per_cta(int heads) {
+    if (heads < 0 || heads > 2) return PA_ERR_INVALID;
+    g_decode_heads.store(heads);
     return PA_OK;
 }
 
@@ -227,6 +234,7 @@ pa_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
     p.v_new = v_new;
     p.new_slots = new_slots;
     p.kernel = g_decode_kernel.load();
+    p.heads_per_cta = g_decode_heads.load();  // 0: the launcher chooses
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
         case PA_F32: return from_cuda(pa::launch_decode_f32(p, st));
@@ -344,6 +352,7 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
     p.max_partitions = ws.partitions < 1 ? 1 : ws.partitions;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.kernel = PA_DECODE_MMA;
+    p.heads_per_cta = g_decode_heads.load();  // 0: the launcher chooses
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

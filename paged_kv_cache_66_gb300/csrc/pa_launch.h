@@ -39,7 +39,8 @@ struct DecodeParams {
     int kernel;                 // pa_decode_kernel choice (PA_DECODE_AUTO / _SIMT / _MMA)
     const float* k_scale;       // FP8 pools: [Hkv] scale of K codes (else null)
     const float* v_scale;       // FP8 pools: [Hkv] scale of V codes (else null)
-    int heads_per_cta;          // tensor-core kernel: KV heads one CTA streams back to back (1 or 2)
+    int heads_per_cta;          // tensor-core kernel: KV heads one CTA streams back to back (1 or 2;
+                                // 0 on entry: the launcher chooses)
     // fused append (16-bit pools, tensor-core kernel): the row of position seq_lens[s] - 1 of
     // every sequence, written by the CTA that streams it (null: plain decode)
     const void* k_new;          // [B, Hkv, D] dtype

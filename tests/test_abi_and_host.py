@@ -104,7 +104,11 @@ def test_kernel_choices_accept_the_declared_values_only():
     for k in (0, 1, 2):
         assert lib.pa_set_decode_kernel(k) == 0
     assert lib.pa_set_decode_kernel(3) == 1
+    for h in (0, 1, 2):
+        assert lib.pa_set_decode_heads_per_cta(h) == 0
+    assert lib.pa_set_decode_heads_per_cta(3) == 1 and lib.pa_set_decode_heads_per_cta(-1) == 1
     assert lib.pa_set_prefill_kernel(0) == 0 and lib.pa_set_decode_kernel(0) == 0
+    assert lib.pa_set_decode_heads_per_cta(0) == 0
 
 
 # ------------------------------------------------------------------ host manager

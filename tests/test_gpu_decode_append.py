@@ -31,11 +31,16 @@ def api():
     return _api
 
 
-@pytest.fixture(params=["simt", "mma"])
+@pytest.fixture(params=["simt", "mma", "mma-h1"])
 def kernel(request, api):
-    api.pa_set_decode_kernel(request.param)
-    yield request.param
+    """Run a decode test once per partition kernel: CUDA cores, tensor cores (KV heads per CTA
+    chosen per launch: two for 16-bit pools), tensor cores with one KV head per CTA forced."""
+    name = request.param
+    api.pa_set_decode_kernel("simt" if name == "simt" else "mma")
+    api.pa_set_decode_heads_per_cta(1 if name == "mma-h1" else 0)
+    yield "simt" if name == "simt" else "mma"
     api.pa_set_decode_kernel("auto")
+    api.pa_set_decode_heads_per_cta(0)
 
 
 def _rand(shape, dtype, gen):

@@ -28,12 +28,16 @@ def api():
     return _api
 
 
-@pytest.fixture(params=["simt", "mma"])
+@pytest.fixture(params=["simt", "mma", "mma-h1"])
 def kernel(request, api):
-    """Run a decode test once per partition kernel (CUDA cores / tensor cores)."""
-    api.pa_set_decode_kernel(request.param)
-    yield request.param
+    """Run a decode test once per partition kernel: CUDA cores, tensor cores (KV heads per CTA
+    chosen per launch: two for 16-bit pools), tensor cores with one KV head per CTA forced."""
+    name = request.param
+    api.pa_set_decode_kernel("simt" if name == "simt" else "mma")
+    api.pa_set_decode_heads_per_cta(1 if name == "mma-h1" else 0)
+    yield "simt" if name == "simt" else "mma"
     api.pa_set_decode_kernel("auto")
+    api.pa_set_decode_heads_per_cta(0)
 
 
 def _rand(shape, dtype, gen):
@@ -202,6 +206,26 @@ def test_simt_and_mma_kernels_agree(api, dtype):
         outs[k] = _run_decode(api, q, K, V, tables, lens, 0.088).double()
     api.pa_set_decode_kernel("auto")
     assert (outs["simt"] - outs["mma"]).abs().max().item() <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_heads_per_cta_does_not_change_results(api, dtype):
+    """One or two KV heads per CTA of the tensor-core kernel: bit-identical outputs (odd Hkv:
+    the last CTA of a pair has one head)."""
+    gen = torch.Generator().manual_seed(31)
+    t, K, V, tables, lens = _setup_paged([1, 300, 513, 1500, 47], 3, 128, 16, dtype, gen)
+    q = _rand((5, 12, 128), dtype, gen)
+    outs = {}
+    try:
+        api.pa_set_decode_kernel("mma")
+        for h in (1, 2, 0):
+            api.pa_set_decode_heads_per_cta(h)
+            outs[h] = _run_decode(api, q, K, V, tables, lens, 128 ** -0.5)
+    finally:
+        api.pa_set_decode_kernel("auto")
+        api.pa_set_decode_heads_per_cta(0)
+    assert torch.equal(outs[1], outs[2]) and torch.equal(outs[1], outs[0])
+    assert api.pa_get_device_error() == 0
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
