@@ -356,7 +356,7 @@ def run_ours(args, ws, rank, local):
             launches += rp.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables,
                                       ds.lens, wsbuf,
                                       events=ev_dec[(j - (args.steps - ev_steps)) * nL + li]
-                                      if j >= args.steps - ev_steps else None)
+                                      if j >= args.steps - ev_steps else None, split=ds.splits[li])
             launches += 1 if wsbuf.numel() else 0
     t_end.record(stream)
     torch.cuda.synchronize()

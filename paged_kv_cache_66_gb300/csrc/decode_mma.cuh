@@ -220,6 +220,31 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
     int* tbl = reinterpret_cast<int*>(smem + C::tbl_off(hpc));
     const int nblk = (tok1 - tok0 + bs - 1) / bs;
     const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks + tok0 / bs;
+    // fused append: the partition holding position L - 1 writes that position's K/V rows of its
+    // heads before any of its copies is issued.  Its loads (slot, table entry, the new rows) are
+    // issued here, beside the table staging, so that they cost one round trip
+    constexpr int VPR = D * static_cast<int>(sizeof(T)) / 16;                  // 16-byte vectors per row
+    constexpr int APP_PER = (2 * 2 * VPR + C::NW * 32 - 1) / (C::NW * 32);  // vectors per thread (<= 2 heads)
+    bool app = false;
+    int64_t app_slot = -1;
+    int app_e = -1;
+    uint4 app_v[APP_PER];
+    if constexpr (!F8) {
+        app = p.new_slots != nullptr && tok1 == L;
+        if (app) {
+            app_slot = __ldg(p.new_slots + s);
+            app_e = __ldg(trow + (L - 1) / bs - tok0 / bs);
+#pragma unroll
+            for (int k = 0; k < APP_PER; ++k) {
+                const int x = tid + k * C::NW * 32;
+                if (x < nh * 2 * VPR) {
+                    const int u = x / (2 * VPR), kind = (x / VPR) & 1, v = x % VPR;
+                    app_v[k] = __ldg(static_cast<const uint4*>(kind ? p.v_new : p.k_new) +
+                                     (static_cast<size_t>(s) * p.hkv + kvh0 + u) * VPR + v);
+                }
+            }
+        }
+    }
     for (int i = tid; i < nblk; i += blockDim.x) {
         int e = __ldg(trow + i);
         if (e < 0 || e >= p.num_blocks) {
@@ -229,28 +254,24 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         tbl[i] = e;
     }
     if constexpr (!F8) {
-        // fused append: the partition holding position L - 1 writes that position's K/V rows
-        // of its heads before any of its copies is issued (the pool stores are fenced against
-        // the async proxy, and the barrier below orders them before the TMA loads)
-        if (p.new_slots != nullptr && tok1 == L) {
-            const int64_t slot = __ldg(p.new_slots + s);
-            if (slot >= 0) {
-                const int e = __ldg(trow + (L - 1) / bs - tok0 / bs);
-                if (e < 0 || e >= p.num_blocks || slot != static_cast<int64_t>(e) * bs + (L - 1) % bs) {
-                    if (tid == 0) flag_error(p.err, PA_DEVERR_SLOT);
-                } else {
-                    constexpr int VPR = D * static_cast<int>(sizeof(T)) / 16;  // 16-byte vectors per row
-                    for (int x = tid; x < nh * 2 * VPR; x += blockDim.x) {
+        // the pool stores are fenced against the async proxy, and the barrier below orders them
+        // before the TMA loads; no other CTA reads position L - 1 of these heads
+        if (app && app_slot >= 0) {
+            const int e = app_e;
+            if (e < 0 || e >= p.num_blocks || app_slot != static_cast<int64_t>(e) * bs + (L - 1) % bs) {
+                if (tid == 0) flag_error(p.err, PA_DEVERR_SLOT);
+            } else {
+#pragma unroll
+                for (int k = 0; k < APP_PER; ++k) {
+                    const int x = tid + k * C::NW * 32;
+                    if (x < nh * 2 * VPR) {
                         const int u = x / (2 * VPR), kind = (x / VPR) & 1, v = x % VPR;
-                        const int h = kvh0 + u;
-                        const uint4* src = static_cast<const uint4*>(kind ? p.v_new : p.k_new) +
-                                           (static_cast<size_t>(s) * p.hkv + h) * VPR + v;
                         uint4* dst = static_cast<uint4*>(const_cast<void*>(kind ? p.v_pool : p.k_pool)) +
-                                     ((static_cast<size_t>(e) * p.hkv + h) * bs + (L - 1) % bs) * VPR + v;
-                        *dst = __ldg(src);
+                                     ((static_cast<size_t>(e) * p.hkv + kvh0 + u) * bs + (L - 1) % bs) * VPR + v;
+                        *dst = app_v[k];
                     }
-                    fence_proxy_async_global();
                 }
+                fence_proxy_async_global();
             }
         }
     }

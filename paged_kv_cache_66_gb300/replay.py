@@ -61,6 +61,7 @@ class DeviceStep:
     q: list                    # per layer [B, Hq, D]
     k_new: list                # per layer [T, Hkv, D]: arrivals' prompt rows, then one row per sequence
     v_new: list
+    splits: list = None        # per layer: the rows split into arrivals and newest rows (views, made once)
 
 
 class Replay:
@@ -109,26 +110,39 @@ class Replay:
             api.pa_decode(out, q, self.k_pools[li], self.v_pools[li], tables, lens, self.wl.scale,
                           partition_tokens=self.partition_tokens, workspace=ws, stream=stream)
 
+    @staticmethod
+    def split_rows(B: int, k_new, v_new, slots):
+        """(arrivals' K, V, slots, newest rows' K, V, slots): views of the step's rows, the
+        arrivals' part None when there are none.  Made once per step outside any timed loop
+        (each view costs the host a few microseconds)."""
+        T = k_new.shape[0]
+        if T == B:
+            return None, None, None, k_new, v_new, slots
+        return k_new[:T - B], v_new[:T - B], slots[:T - B], k_new[T - B:], v_new[T - B:], slots[T - B:]
+
     def step_layer(self, li: int, out, q, k_new, v_new, slots, tables, lens, workspace, stream=None,
-                   events=None) -> int:
+                   events=None, split=None) -> int:
         """One layer of a decode step: the step's rows into the pool, then the
         decode.  k_new / v_new / slots hold the arrivals' prompt rows first, then
         one row per sequence (its newest position); with `fused` those last B rows
-        go with the decode in one pa_decode_append.  `events` (a pair) brackets the
-        decode launch.  Returns the number of launches made (merge not counted)."""
-        B, T = q.shape[0], k_new.shape[0]
+        go with the decode in one pa_decode_append (`split`: split_rows of them, if
+        already made).  `events` (a pair) brackets the decode launch.  Returns the
+        number of launches made (merge not counted)."""
         launches = 0
         if not self.fused:
             self.append(li, k_new, v_new, slots, stream=stream)
             launches += 1
-        elif T > B:
-            self.append(li, k_new[:T - B], v_new[:T - B], slots[:T - B], stream=stream)
-            launches += 1
+        else:
+            k_arr, v_arr, s_arr, k_last, v_last, s_last = (split if split is not None else
+                                                           self.split_rows(q.shape[0], k_new, v_new, slots))
+            if k_arr is not None:
+                self.append(li, k_arr, v_arr, s_arr, stream=stream)
+                launches += 1
         if events is not None:
             events[0].record(stream if stream is not None else torch.cuda.current_stream())
         if self.fused:
             ws = workspace if workspace is not None and workspace.numel() else None
-            api.pa_decode_append(out, q, k_new[T - B:], v_new[T - B:], slots[T - B:], self.k_pools[li],
+            api.pa_decode_append(out, q, k_last, v_last, s_last, self.k_pools[li],
                                  self.v_pools[li], tables, lens, self.wl.scale, partition_tokens=self.partition_tokens,
                                  workspace=ws, stream=stream)
         else:
@@ -238,8 +252,11 @@ class Replay:
             q.append(wcfg.q_rows(wl, layer, plan.step, rows, device=dev))
             kn.append(wcfg.kv_rows(wl, layer, "k", all_owners, all_pos, device=dev))
             vn.append(wcfg.kv_rows(wl, layer, "v", all_owners, all_pos, device=dev))
-        return DeviceStep(plan, torch.as_tensor(all_slots).to(dev), torch.as_tensor(all_pairs).to(dev),
-                          torch.as_tensor(plan.tables).to(dev), torch.as_tensor(plan.lens).to(dev), q, kn, vn)
+        d_slots = torch.as_tensor(all_slots).to(dev)
+        B = len(plan.uids)
+        splits = [self.split_rows(B, k, v, d_slots) for k, v in zip(kn, vn)]
+        return DeviceStep(plan, d_slots, torch.as_tensor(all_pairs).to(dev),
+                          torch.as_tensor(plan.tables).to(dev), torch.as_tensor(plan.lens).to(dev), q, kn, vn, splits)
 
     def workspace_for(self, batch: int, max_blocks: int) -> torch.Tensor:
         wl = self.wl
@@ -259,5 +276,5 @@ class Replay:
             outs = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
         for li in range(len(self.layers)):
             self.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables, ds.lens, ws,
-                            stream=stream)
+                            stream=stream, split=ds.splits[li] if ds.splits else None)
         return outs
