@@ -560,7 +560,7 @@ def run_op(args, local):
                               "peak_kind": f"{peak_kind} hbm_gbs"})
     elif args.op == "prefill":
         api.pa_set_prefill_kernel(args.prefill_kernel)
-        wl = wcfg.prefill_config(dtype=args.prefill_dtype)
+        wl = wcfg.prefill_config(dtype=args.prefill_dtype, head_dim=args.prefill_head_dim)
         kp, vp, q = wcfg.prefill_inputs(wl, device=dev)
         tables = torch.as_tensor(wl.tables(), device=dev)
         lens = torch.full((wl.batch,), wl.length, dtype=torch.int32, device=dev)
@@ -644,6 +644,8 @@ def main():
     ap.add_argument("--copy-layers", type=int, default=32, help="--op copy: layers (pools of 4096 blocks each)")
     ap.add_argument("--copy-pairs", type=int, default=64, help="--op copy: copy-on-write pairs")
     ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc05", "tc05w"], help="--op prefill kernel")
+    ap.add_argument("--prefill-head-dim", type=int, default=128, choices=[64, 128, 256],
+                    help="--op prefill head dim (Hq 32, Hkv 8 kept)")
     ap.add_argument("--prefill-dtype", default="bf16", choices=["f16", "bf16"], help="--op prefill storage dtype")
     ap.add_argument("--op", default="step", choices=["step", "append", "copy", "host", "prefill"],
                     help="step = the benchmark line; others measure one row of the path alone")

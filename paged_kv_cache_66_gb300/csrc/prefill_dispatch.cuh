@@ -1,11 +1,13 @@
 // Choice between the prefill kernels for one pa_prefill call: the tcgen05
-// kernels for D in {64, 128} (128-key tiles, prefill_tc05w.cuh, at D = 128;
-// 64-key tiles, prefill_tc05.cuh, at D = 64 or when forced) unless the caller
-// forced the warp-level one (prefill_mma.cuh), which covers every D.
+// kernels (128-key tiles, prefill_tc05w.cuh, at D = 128; 64-key tiles,
+// prefill_tc05.cuh, at D = 64 or when forced at D = 128; one query tile with Q
+// in tensor memory, prefill_tc05d.cuh, at D = 256) unless the caller forced the
+// warp-level one (prefill_mma.cuh), which covers every D.
 #pragma once
 
 #include "prefill_mma.cuh"
 #include "prefill_tc05.cuh"
+#include "prefill_tc05d.cuh"
 #include "prefill_tc05w.cuh"
 
 namespace pa {
@@ -21,7 +23,8 @@ cudaError_t launch_prefill_path(const PrefillParams& p, const CUtensorMap& km, c
         if (p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
         if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05<T, D, G>(p, km, vm, max_q, stream);
     } else {
-        if (p.kernel == PA_PREFILL_TC05 || p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
+        if (p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
+        if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05d<T, G>(p, km, vm, max_q, stream);
     }
     return launch_prefill<T, D, G>(p, km, vm, max_q, stream);
 }

@@ -95,6 +95,9 @@ CASES = [
     (6, 3, 128, 16, [200, 90], [100, 90]),              # odd Hkv
     (16, 2, 128, 16, [1500, 777], [300, 777]),          # G = 8: many 128-key tiles, ragged ends
     (8, 2, 128, 256, [900], [400]),                     # b = 256 at D = 128
+    (8, 2, 256, 16, [700, 150], [300, 150]),            # D = 256, G = 4: history + ragged chunk
+    (4, 4, 256, 16, [300], [300]),                      # D = 256, G = 1: three 128-row CTAs
+    (8, 4, 256, 32, [1000], [257]),                     # D = 256, G = 2, b = 32
 ]
 
 
@@ -109,7 +112,7 @@ def kernel(request, api):
 @pytest.mark.parametrize("case", CASES)
 def test_prefill_matches_oracle(api, kernel, dtype, case):
     Hq, Hkv, D, b, lengths, chunks = case
-    if (kernel == "tc05" and D == 256) or (kernel == "tc05w" and D != 128):
+    if kernel == "tc05w" and D != 128:
         K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype, seed=1)
         with pytest.raises(api.PagedKVError) as e:
             _run(api, K, V, q, tables, lens, qstart, 0.1)

@@ -288,9 +288,12 @@ class PrefillWorkload:
         return self.batch * (C * H + C * (C + 1) // 2)
 
 
-def prefill_config(dtype: str = "bf16", batch: int = 8, history: int = 3072, chunk: int = 1024) -> PrefillWorkload:
+def prefill_config(dtype: str = "bf16", batch: int = 8, history: int = 3072, chunk: int = 1024,
+                   head_dim: int = 128) -> PrefillWorkload:
+    """The Llama-3-8B layer shape (Hq 32, Hkv 8, D 128); other head dims keep the head counts."""
     per = -(-(history + chunk) // 16)
-    return PrefillWorkload(f"prefill-llama8b-{dtype}-b{batch}-h{history}-c{chunk}", Hq=32, Hkv=8, D=128, b=16,
+    shape = "llama8b" if head_dim == 128 else f"hq32-hkv8-d{head_dim}"
+    return PrefillWorkload(f"prefill-{shape}-{dtype}-b{batch}-h{history}-c{chunk}", Hq=32, Hkv=8, D=head_dim, b=16,
                            dtype=dtype, batch=batch, history=history, chunk=chunk,
                            num_blocks=max(4096, batch * per + 64), seed=1006)
 
