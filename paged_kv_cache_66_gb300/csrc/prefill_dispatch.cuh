@@ -1,8 +1,8 @@
 // Choice between the prefill kernels for one pa_prefill call: the tcgen05
-// kernels (128-key tiles, prefill_tc05w.cuh, at D = 128; 64-key tiles,
-// prefill_tc05.cuh, at D = 64 or when forced at D = 128; one query tile with Q
-// in tensor memory, prefill_tc05d.cuh, at D = 256) unless the caller forced the
-// warp-level one (prefill_mma.cuh), which covers every D.
+// kernels (128-key tiles, prefill_tc05w.cuh, at D in {64, 128}; 64-key tiles,
+// prefill_tc05.cuh, when forced; one query tile with Q in tensor memory,
+// prefill_tc05d.cuh, at D = 256) unless the caller forced the warp-level one
+// (prefill_mma.cuh), which covers every D.
 #pragma once
 
 #include "prefill_mma.cuh"
@@ -15,12 +15,11 @@ namespace pa {
 template <typename T, int D, int G>
 cudaError_t launch_prefill_path(const PrefillParams& p, const CUtensorMap& km, const CUtensorMap& vm, int max_q,
                                 cudaStream_t stream) {
-    if constexpr (D == 128) {
+    if constexpr (D <= 128) {
         if (p.kernel == PA_PREFILL_TC05W || p.kernel == PA_PREFILL_AUTO)
-            return launch_prefill_tc05w<T, G>(p, km, vm, max_q, stream);
+            return launch_prefill_tc05w<T, D, G>(p, km, vm, max_q, stream);
     }
     if constexpr (D <= 128) {
-        if (p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
         if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05<T, D, G>(p, km, vm, max_q, stream);
     } else {
         if (p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;

@@ -1,12 +1,12 @@
-// Paged prefill on tcgen05 with 128-key K/V tiles (D = 128): the same operation,
+// Paged prefill on tcgen05 with 128-key K/V tiles (D in {64, 128}): the same operation,
 // row packing and softmax arithmetic as prefill_tc05.cuh ("25. Paged attention
 // and prefix caching", stretch exercise 4; "Chapter 7 Paged KV Cache and Memory
 // Management", 4.1 step 3), laid out so that the score MMAs run at N = 128.
 //
 // One CTA owns 256 query rows of one KV head as two 128-row tiles X = A, B that
 // share every 128-key K/V tile j.  Tensor memory holds O_A, O_B and one S buffer
-// per tile (4 x 128 columns); P_Xj (two 16-bit values per column) overwrites the
-// first 64 columns of S_X.  The MMA issuer keeps one fixed order:
+// per tile (2 D + 2 x 128 columns); P_Xj (two 16-bit values per column) overwrites
+// the first 64 columns of S_X.  The MMA issuer keeps one fixed order:
 //   O_A += P_Aj V_j,  S_A(j+1) = Q_A K_(j+1)^T,  O_B += P_Bj V_j,  S_B(j+1) = Q_B K_(j+1)^T
 // so the softmax of one tile overlaps the other tile's MMAs.  S_X(j+1) follows
 // P_Xj . V_j on the tensor pipe, which performs one thread's MMAs in issue order;
@@ -14,7 +14,7 @@
 // thread done, so the softmax may rescale O_X (no P . V of tile X in flight) as
 // soon as it sees S_X(j+1).
 //
-// K and V slots (two of each, 32 KiB per 128-key tile) are released separately:
+// K and V slots (two of each, 128 keys x D per tile) are released separately:
 // K_j once both S_j have completed, V_j once both P . V_j have, each refilled by
 // its own producer warp; every slot then has about two iterations to land.
 // Warps: 0-15 softmax (group X = warp / 8; two threads per row, one per 64-key
@@ -54,13 +54,15 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
 
 }  // namespace tc05
 
+template <int D_>
 struct Tc05wCfg {
-    static constexpr int D = 128, BM = 256, BN = 128;
+    static constexpr int D = D_, BM = 256, BN = 128;
+    static_assert(D == 64 || D == 128, "D in {64, 128}");
     static constexpr int NBOX = D / 64;              // 64-dim (128-byte) boxes per row
     static constexpr int QBOX = 128 * 128;           // 128 rows x 128 B
-    static constexpr int Q_BYTES = 2 * NBOX * QBOX;  // both tiles: 64 KiB
+    static constexpr int Q_BYTES = 2 * NBOX * QBOX;  // both tiles
     static constexpr int KV_BOX = BN * 128;          // 128 keys x 128 B
-    static constexpr int SLOT_BYTES = NBOX * KV_BOX; // one K or V tile: 32 KiB
+    static constexpr int SLOT_BYTES = NBOX * KV_BOX; // one K or V tile
     static constexpr int SLOTS = 2;                  // per operand
     static constexpr int K_OFF = Q_BYTES;
     static constexpr int V_OFF = K_OFF + SLOTS * SLOT_BYTES;
@@ -70,7 +72,7 @@ struct Tc05wCfg {
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int RED_OFF = MISC_OFF + 64;  // row max exchange [2][2][2][128], row sums [2][2][128]
     static constexpr size_t smem_bytes = 1024 + RED_OFF + (8 + 4) * 128 * 4;
-    // tensor memory: O_A [0, 128), O_B [128, 256), S_A [256, 384), S_B [384, 512)
+    // tensor memory: O_A [0, D), O_B [D, 2D), S_A [2D, 2D + 128), S_B [2D + 128, 2D + 256)
     static constexpr int O_COL = 0, S_COL = 2 * D;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NSW = 16;  // two groups of eight: two threads (key halves) per row
@@ -79,12 +81,13 @@ struct Tc05wCfg {
     static constexpr int SUB = BN / 16;  // 16-key sub-tiles (one block row each) per tile
 };
 
-template <typename T, int G>
-__global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
+template <typename T, int D_, int G>
+__global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
     prefill_tc05w(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
-    using C = Tc05wCfg;
+    using C = Tc05wCfg<D_>;
     constexpr int D = C::D, NBOX = C::NBOX, BN = C::BN, SLOTS = C::SLOTS, SUB = C::SUB;
+    constexpr int DH = D / 2;  // O columns (dims) per thread of a row
     constexpr int QT = C::BM / G;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
     const int warp_tok = tok0 + (X * 128 + wq * 32) / G;
     const int warp_pos_min = warp_tok < Cq ? base + warp_tok : -1;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t o_addr = lane_addr + C::O_COL + X * D + hh * 64;
+    const uint32_t o_addr = lane_addr + C::O_COL + X * D + hh * DH;
     const uint32_t sa = lane_addr + C::S_COL + X * BN;
     float* xmax = reinterpret_cast<float*>(smem + C::RED_OFF);  // [tile parity][X][half][row]
     float* xl = xmax + 2 * 2 * 2 * 128;                          // [X][half][row]
@@ -301,13 +304,13 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
     {
         // this half of the Q row into tile X's K-major swizzled operand (zeros past the chunk)
         const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                           (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D) +
-                            hh * 8;
-        unsigned char* qx = smem + X * NBOX * C::QBOX + hh * C::QBOX;
+                                                           (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D);
+        unsigned char* qx = smem + X * NBOX * C::QBOX;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 v = valid ? __ldg(qrow + c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(qx + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        for (int i = 0; i < D / 16; ++i) {
+            const int cc = hh * (D / 16) + i, bx = cc >> 3, c = cc & 7;  // 16-byte chunk of the row
+            const uint4 v = valid ? __ldg(qrow + cc) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(qx + bx * C::QBOX + r * 128 + ((c ^ (r & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
         mbar_arrive(q_full);
@@ -374,7 +377,7 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
         const float a = scale_o ? tc05::fast_exp2(m - mx) : 1.f;
         if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
+            for (int c0 = 0; c0 < DH; c0 += 32) {
                 uint32_t o[32];
                 tc05::ld32(o_addr + c0, o);
                 tc05::wait_ld();
@@ -435,9 +438,9 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
     if (__all_sync(0xffffffffu, done)) {
         tc05::fence_after();
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + hh * 64;
+        T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D + hh * DH;
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        for (int c0 = 0; c0 < DH; c0 += 32) {
             uint32_t o[32];
             tc05::ld32(o_addr + c0, o);
             tc05::wait_ld();
@@ -460,20 +463,20 @@ __global__ void __launch_bounds__(Tc05wCfg::THREADS, 1)
     tc05::named_sync(1, (C::NSW + 1) * 32);
 }
 
-template <typename T, int G>
+template <typename T, int D, int G>
 cudaError_t launch_prefill_tc05w(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  int max_query_len, cudaStream_t stream) {
-    using C = Tc05wCfg;
+    using C = Tc05wCfg<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc05w<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc05w<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(C::smem_bytes));
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int64_t rows = static_cast<int64_t>(max_query_len) * G;
     const unsigned tiles = static_cast<unsigned>((rows + C::BM - 1) / C::BM);
-    return launch_pdl(prefill_tc05w<T, G>, dim3(tiles, p.hkv, p.batch), dim3(C::THREADS), C::smem_bytes, stream, p,
+    return launch_pdl(prefill_tc05w<T, D, G>, dim3(tiles, p.hkv, p.batch), dim3(C::THREADS), C::smem_bytes, stream, p,
                       kmap, vmap);
 }
 
