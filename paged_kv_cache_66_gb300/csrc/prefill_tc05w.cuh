@@ -14,7 +14,7 @@
 // thread done, so the softmax may rescale O_X (no P . V of tile X in flight) as
 // soon as it sees S_X(j+1).
 //
-// K and V slots (two of each, 128 keys x D per tile) are released separately:
+// K and V slots (two of each at D = 128, three at D = 64; 128 keys x D per tile) are released separately:
 // K_j once both S_j have completed, V_j once both P . V_j have, each refilled by
 // its own producer warp; every slot then has about two iterations to land.
 // Warps: 0-15 softmax (group X = warp / 8; two threads per row, one per 64-key
@@ -63,7 +63,11 @@ struct Tc05wCfg {
     static constexpr int Q_BYTES = 2 * NBOX * QBOX;  // both tiles
     static constexpr int KV_BOX = BN * 128;          // 128 keys x 128 B
     static constexpr int SLOT_BYTES = NBOX * KV_BOX; // one K or V tile
-    static constexpr int SLOTS = 2;                  // per operand
+#ifdef PA_TC05W_SLOTS64
+    static constexpr int SLOTS = D == 64 ? PA_TC05W_SLOTS64 : 2;  // build-time override (tuning sweeps)
+#else
+    static constexpr int SLOTS = D == 64 ? 3 : 2;  // per operand (as many as shared memory holds at D = 128)
+#endif
     static constexpr int K_OFF = Q_BYTES;
     static constexpr int V_OFF = K_OFF + SLOTS * SLOT_BYTES;
     static constexpr int BAR_OFF = V_OFF + SLOTS * SLOT_BYTES;
