@@ -163,6 +163,25 @@ def test_prefill_bad_table_entry_is_flagged(api, kernel):
     assert api.pa_get_device_error() == 2                 # PA_DEVERR_TABLE
 
 
+def test_prefill_d256_bad_entries_are_flagged_and_skipped(api):
+    """The D = 256 tcgen05 kernel's error paths: an inconsistent chunk is skipped (rows stay
+    unwritten) and flagged, the other sequence still matches the oracle; a table entry outside
+    the pool is flagged."""
+    Hq, Hkv, D, b = 8, 2, 256, 16
+    K, V, q, tables, lens, qstart = _setup([20, 90], [5, 40], Hq, Hkv, D, b, torch.bfloat16, seed=41)
+    lens[0] = 3                                           # chunk of 5 > length 3
+    got = _run(api, K, V, q, tables, lens, qstart, 0.0625)
+    assert api.pa_get_device_error() == 4                 # PA_DEVERR_SEQLEN
+    assert torch.isnan(got[:5]).all()
+    want = oprefill.paged_prefill_batch(q[5:].double().numpy(), K.double().numpy(), V.double().numpy(),
+                                        tables[1:].tolist(), lens[1:].tolist(), [0, 40], b, 0.0625)
+    _check(got[5:].double().numpy(), want, V.double().numpy(), torch.bfloat16, _visible([90], [40]))
+    K, V, q, tables, lens, qstart = _setup([70], [70], Hq, Hkv, D, b, torch.bfloat16, seed=42)
+    tables[0, 2] = K.shape[0] + 3
+    _run(api, K, V, q, tables, lens, qstart, 0.0625)
+    assert api.pa_get_device_error() == 2                 # PA_DEVERR_TABLE
+
+
 def test_prefill_f32_unsupported(api):
     K, V, q, tables, lens, qstart = _setup([20], [20], 4, 2, 64, 16, torch.float32, seed=13)
     with pytest.raises(api.PagedKVError) as e:
