@@ -221,7 +221,7 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const 
  * pa_decode_fp8 -- like pa_decode over FP8 pools: q and out [B, Hq, D] in
  *   `q_dtype` (f16 or bf16); the attention is taken over the dequantised
  *   history, with q used in f16 (exact for bf16 values in f16's normal range)
- *   and fp32 accumulation.  Tensor-core kernel only: D in {128, 256}, Hq/Hkv in
+ *   and fp32 accumulation.  Tensor-core kernel only: D in {64, 128, 256}, Hq/Hkv in
  *   {1, 2, 4, 8}, b a multiple of 16, num_blocks * Hkv * b < 2^31 (else
  *   PA_ERR_UNSUPPORTED).  Workspace as for pa_decode.
  */

@@ -55,14 +55,17 @@ cudaError_t dispatch_decode(const DecodeParams& p, cudaStream_t stream) {
 
 namespace pa {
 
-// FP8 (E4M3) pools: the tensor-core kernel with byte tiles; D a multiple of 128.
+// FP8 (E4M3) pools: the tensor-core kernel with byte tiles; D = 64 as lines of two 64-byte rows
+// (16 tokens = 8 lines of 128 bytes), D = 128, 256 as 128-byte boxes.
 template <typename T, int D>
 cudaError_t dispatch_fp8_group(const DecodeParams& p, cudaStream_t stream) {
     const uint64_t rows = static_cast<uint64_t>(p.num_blocks) * p.hkv * p.block_size;
     if (rows >= (1ull << 31)) return cudaErrorNotSupported;
     CUtensorMap km, vm;
-    if (!encode_pool_tmap(&km, p.k_pool, rows, D, 1) || !encode_pool_tmap(&vm, p.v_pool, rows, D, 1))
-        return cudaErrorInvalidValue;
+    const bool ok = D == 64 ? encode_pool_tmap(&km, p.k_pool, rows / 2, 128, 1, 8) &&
+                                  encode_pool_tmap(&vm, p.v_pool, rows / 2, 128, 1, 8)
+                            : encode_pool_tmap(&km, p.k_pool, rows, D, 1) && encode_pool_tmap(&vm, p.v_pool, rows, D, 1);
+    if (!ok) return cudaErrorInvalidValue;
     switch (p.hq / p.hkv) {
         case 1: return launch_mma<T, uint8_t, D, 1>(p, km, vm, stream);
         case 2: return launch_mma<T, uint8_t, D, 2>(p, km, vm, stream);
@@ -75,6 +78,7 @@ cudaError_t dispatch_fp8_group(const DecodeParams& p, cudaStream_t stream) {
 template <typename T>
 cudaError_t dispatch_decode_fp8(const DecodeParams& p, cudaStream_t stream) {
     switch (p.d) {
+        case 64: return dispatch_fp8_group<T, 64>(p, stream);
         case 128: return dispatch_fp8_group<T, 128>(p, stream);
         case 256: return dispatch_fp8_group<T, 256>(p, stream);
         default: return cudaErrorNotSupported;

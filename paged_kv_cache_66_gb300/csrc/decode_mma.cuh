@@ -132,11 +132,13 @@ struct MmaCfg {
     static constexpr bool F8 = EB == 1;
     static constexpr int TILE = 16;                    // tokens per tile (M of the score MMA)
     static constexpr int ROW_BYTES = D * EB;
-    static_assert(ROW_BYTES % 128 == 0, "rows of whole 128-byte boxes");
-    static constexpr int NBOX = ROW_BYTES / 128;       // 128-byte boxes per 16-token row block
+    // 64-byte rows (E4M3 at D = 64): two tokens share one 128-byte swizzled line
+    static constexpr bool PAIR = ROW_BYTES == 64;
+    static_assert(PAIR || ROW_BYTES % 128 == 0, "rows of whole 128-byte boxes, or token pairs");
+    static constexpr int NBOX = PAIR ? 1 : ROW_BYTES / 128;  // 128-byte boxes per 16-token row block
     static constexpr int BOX_ELEMS = 128 / EB;
     static constexpr int CHUNKS = ROW_BYTES / 16;      // 16-byte chunks per row
-    static constexpr int BOX_BYTES = TILE * 128;       // 2 KiB, 1024-byte aligned in smem
+    static constexpr int BOX_BYTES = TILE * 128 / (PAIR ? 2 : 1);  // 1024-byte aligned in smem
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
     // 2 stages x 4 warps (2 warps when a stage is >= 16 KiB; 3 stages for the
@@ -174,9 +176,17 @@ struct MmaCfg {
 };
 
 // Byte offset of (token row r, 16-byte chunk c) of a tile stored as NBOX boxes
-// of 16 rows x 128 bytes with the 128-byte swizzle (chunk index XOR row % 8).
+// of 16 rows x 128 bytes with the 128-byte swizzle (chunk index XOR row % 8);
+// with PAIR (64-byte rows) as 8 lines of two tokens, token r at line r / 2,
+// chunks 4 (r % 2) + c, the line index doing the swizzle.
+template <bool PAIR = false>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
-    return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    if constexpr (PAIR) {
+        const int line = r >> 1;
+        return static_cast<uint32_t>(line * 128 + ((((r & 1) * 4 + c) ^ (line & 7)) << 4));
+    } else {
+        return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
 }
 
 template <typename T, typename PE, int D, int G>
@@ -302,8 +312,10 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         mbar_arrive_expect_tx(&bars[st], 2 * C::TILE_BYTES);
 #pragma unroll
         for (int bx = 0; bx < C::NBOX; ++bx) {
-            tma_load_2d(dst + bx * C::BOX_BYTES, &kmap, bx * C::BOX_ELEMS, row, &bars[st]);
-            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &vmap, bx * C::BOX_ELEMS, row, &bars[st]);
+            // token pairs: the maps view the pool as lines of two rows (row is even: b % 16 == 0)
+            const int y = C::PAIR ? row >> 1 : row;
+            tma_load_2d(dst + bx * C::BOX_BYTES, &kmap, bx * C::BOX_ELEMS, y, &bars[st]);
+            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &vmap, bx * C::BOX_ELEMS, y, &bars[st]);
         }
     };
     if (lane == 0)
@@ -377,7 +389,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
 #pragma unroll
                     for (int ks = 0; ks < KSTEPS; ks += 2) {
                         uint32_t r[4], a0[4], a1[4];
-                        ldsm_x4(kbase + swz(lr + (lm & 1) * 8, ks + (lm >> 1)), r);
+                        ldsm_x4(kbase + swz<C::PAIR>(lr + (lm & 1) * 8, ks + (lm >> 1)), r);
                         // lane holds dims 4t..4t+3 of rows g and g+8: {r0 lo, r1 lo, r0 hi, r1 hi} per k-step
                         e4m3x4_to_h2x2(r[0], a0[0], a0[2]);
                         e4m3x4_to_h2x2(r[1], a0[1], a0[3]);
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                     // unwritten slots of the tail may hold anything (NaN * 0 = NaN): zero those V rows
                     for (int e = lane; e < (C::TILE - nv) * C::CHUNKS; e += 32) {
                         const int r = nv + e / C::CHUNKS, c = e % C::CHUNKS;
-                        *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vt + swz<C::PAIR>(r, c)) = make_uint4(0u, 0u, 0u, 0u);
                     }
                     __syncwarp();
                 }
@@ -450,7 +462,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
 #pragma unroll
                     for (int mt = 0; mt < KSTEPS; mt += 2) {
                         uint32_t r[4], a0[4], a1[4];
-                        ldsm_x4_t(vbase + swz(lr + (lm & 1) * 8, mt + (lm >> 1)), r);
+                        ldsm_x4_t(vbase + swz<C::PAIR>(lr + (lm & 1) * 8, mt + (lm >> 1)), r);
                         // r[i] bytes: (tok 2t, dim 2g), (tok 2t, dim 2g+1), (tok 2t+1, dim 2g), (tok 2t+1, dim 2g+1);
                         // one byte permute groups each dim's two tokens: [b0 b2 | b1 b3]
                         e4m3x4_to_h2x2(__byte_perm(r[0], 0u, 0x3120u), a0[0], a0[1]);

@@ -85,7 +85,7 @@ WsLayout ws_layout(int batch, int hq, int d, int max_blocks, int b, int part) {
 
 namespace pa {
 
-bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes) {
+bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes, int box_rows) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q{};
@@ -97,7 +97,7 @@ bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, 
     if (!g_encode) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * elt_bytes};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt_bytes), 16};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt_bytes), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(map, elt_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -314,7 +314,7 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
     const int group = num_q_heads / num_kv_heads;
     if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
-    if (head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
     if (static_cast<uint64_t>(num_blocks) * num_kv_heads * block_size >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
     const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;

@@ -85,7 +85,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // 2-D TMA descriptor of a pool viewed as [rows, D] elements of `elt_bytes`
 // (2, or 1 for FP8), boxes of 16 rows x 128 bytes with the 128-byte swizzle.
-bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes);
+// 2-D map over a pool viewed as `rows` rows of `d` elements: boxes of 128 bytes x box_rows rows,
+// 128-byte swizzle
+bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes, int box_rows = 16);
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slots,
                              int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,
