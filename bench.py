@@ -20,6 +20,7 @@ independent K/V, fp16, Hq 32 / Hkv 8 / D 128, b 16, 512-token partitions.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -344,6 +345,8 @@ def run_ours(args, ws, rank, local):
     clocks = ClockSampler(local)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
+    gc.collect()
+    gc.disable()  # no collector pause inside the timed region
     t_start.record(stream)
     for j in range(args.steps):
         ds = dsteps[args.warmup + j]
@@ -360,6 +363,7 @@ def run_ours(args, ws, rank, local):
             launches += 1 if wsbuf.numel() else 0
     t_end.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     _barrier(ws)
     clk = clocks.stop()
     dev_ms = t_start.elapsed_time(t_end)
@@ -421,8 +425,10 @@ def run_e2e(args, wl, rp, dev, ws):
 
     Per step: the C++ plan writes slots / lengths / tables into one pinned
     metadata buffer (one host->device copy); the step's q, new K and new V rows
-    of every layer sit in one pinned buffer (one host->device copy); every
-    layer's output lands in one device buffer read back with one copy.
+    of every layer are copied on the host into one pinned staging buffer (one
+    host->device copy); every layer's output lands in one device buffer read
+    back with one copy.  The pinned buffers form a small ring, each reused once
+    its uploads are done, so the host works a few steps ahead of the device.
     """
     from paged_kv_cache_66_gb300 import api
     from workload import configs as wc
@@ -442,7 +448,7 @@ def run_e2e(args, wl, rp, dev, ws):
             x[li, :nq] = wc.q_rows(wl, layer, rp.steps_done + j, np.arange(B)).reshape(-1)
             x[li, nq:nq + nk] = wc.kv_rows(wl, layer, "k", owners, pos).reshape(-1)
             x[li, nq + nk:] = wc.kv_rows(wl, layer, "v", owners, pos).reshape(-1)
-        host_in.append(x.pin_memory())
+        host_in.append(x)
     stride = max(len(rp.host.table(u)) for u in uids) + args.steps // wl.b + 2
     meta_bytes = B * 8 + B * 4 + B * stride * 4
 
@@ -450,8 +456,11 @@ def run_e2e(args, wl, rp, dev, ws):
         return (buf[:B * 8].view(torch.int64), buf[B * 8:B * 12].view(torch.int32),
                 buf[B * 12:].view(torch.int32).view(B, stride))
 
-    # two pinned metadata buffers, reused every other step once their upload is done
-    bufs = [{"meta": torch.zeros(meta_bytes, dtype=torch.uint8).pin_memory(), "ev": None} for _ in range(2)]
+    # a ring of pinned metadata buffers, each reused once its upload is done: the host may run up
+    # to that many steps ahead of the device, so a host pause shorter than that costs nothing
+    NMETA = 4
+    bufs = [{"meta": torch.zeros(meta_bytes, dtype=torch.uint8).pin_memory(),
+             "x": torch.empty((nL, row), dtype=wl.torch_dtype).pin_memory(), "ev": None} for _ in range(NMETA)]
     d_meta = torch.empty(meta_bytes, dtype=torch.uint8, device=dev)
     d_slots, d_lens, d_tables = meta_views(d_meta)
     d_x = torch.empty((nL, row), dtype=wl.torch_dtype, device=dev)
@@ -467,9 +476,11 @@ def run_e2e(args, wl, rp, dev, ws):
     kv = 0
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    gc.collect()
+    gc.disable()  # no collector pause inside the timed region
     t0.record(stream)
     for j in range(args.steps):
-        buf = bufs[j % 2]
+        buf = bufs[j % NMETA]
         if buf["ev"] is not None:
             buf["ev"].synchronize()
         slots, lens, tables = meta_views(buf["meta"])
@@ -477,15 +488,16 @@ def run_e2e(args, wl, rp, dev, ws):
         pairs, width = rp.host.decode_step(uids, tables.numpy(), ln, slots.numpy())
         kv += _kv_bytes(wl, ln, rp.kv_elt) * nL
         d_meta.copy_(buf["meta"], non_blocking=True)
-        buf["ev"] = torch.cuda.Event()
-        buf["ev"].record(stream)
         h2d += meta_bytes
         if len(pairs):
-            d_pairs = torch.as_tensor(pairs).to(dev, non_blocking=False)
+            d_pairs = torch.as_tensor(pairs).pin_memory().to(dev, non_blocking=True)
             api.pa_copy_blocks(rp.k_pools, rp.v_pools, d_pairs)
             h2d += pairs.nbytes
-        d_x.copy_(host_in[j], non_blocking=True)
-        h2d += host_in[j].numel() * wl.elt
+        buf["x"].copy_(host_in[j])  # the step's inputs into pinned staging memory (host copy)
+        d_x.copy_(buf["x"], non_blocking=True)
+        buf["ev"] = torch.cuda.Event()
+        buf["ev"].record(stream)  # both uploads from this ring slot are done past this point
+        h2d += buf["x"].numel() * wl.elt
         wsbuf = rp.workspace_for(B, stride)
         for li in range(nL):
             rp.step_layer(li, d_out[li], d_q[li], d_k[li], d_v[li], d_slots, d_tables, d_lens, wsbuf)
@@ -493,6 +505,7 @@ def run_e2e(args, wl, rp, dev, ws):
         d2h += d_out.numel() * wl.elt
     t1.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     rp.steps_done += args.steps
     ms = _max_over_ranks(t0.elapsed_time(t1), ws, dev)
     kv_all = _sum_over_ranks(float(kv), ws, dev)
