@@ -56,6 +56,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 2^x on the MUFU unit (relative error ~2^-22; -inf -> +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -296,18 +303,28 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
     unsigned char* ring = smem + warp * STAGES * C::STAGE_BYTES;
     const int my_n = warp < n_tiles ? (n_tiles - warp + NW - 1) / NW : 0;
     const int my_total = nh * my_n;  // this warp's tiles over all heads: one stream through its ring
+    // tile i of the partition lies in table entry i / tpb (the partition starts on a block
+    // boundary); i < 512 and tpb <= 16, where (i * inv_tpb) >> 16 is that quotient exactly
+    const int tpb = bs / C::TILE;
+    const uint32_t inv_tpb = (65536u + tpb - 1) / tpb;
 
-    // tile jj of the stream: head jj / my_n, the warp's (jj % my_n)-th tile of the partition
+    // tile jj of the stream: head jj / my_n, the warp's (jj % my_n)-th tile of the partition.
+    // Copies go out in stream order, so lane 0 steps (iss_u, iss_j) instead of dividing.
+    int iss_u = 0, iss_j = 0;
     auto issue = [&](int jj) {
-        const int u = jj / my_n, j = jj - u * my_n;
-        const int i = warp + j * NW;
+        const int u = iss_u, i = warp + iss_j * NW;
+        if (++iss_j == my_n) {
+            iss_j = 0;
+            ++iss_u;
+        }
         const int st = jj % STAGES;
-        const int blk = tbl[(i * C::TILE) / bs];
+        const int bi = static_cast<int>((static_cast<uint32_t>(i) * inv_tpb) >> 16);
+        const int blk = tbl[bi];
         if (blk < 0) {
             mbar_arrive_expect_tx(&bars[st], 0);
             return;
         }
-        const int row = (blk * p.hkv + kvh0 + u) * bs + (i * C::TILE) % bs;
+        const int row = (blk * p.hkv + kvh0 + u) * bs + (i - bi * tpb) * C::TILE;
         unsigned char* dst = ring + st * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[st], 2 * C::TILE_BYTES);
 #pragma unroll
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
             }
             const int i = warp + j * NW;
             const int nv = min(C::TILE, tok1 - (tok0 + i * C::TILE));
-            const bool present = tbl[(i * C::TILE) / bs] >= 0;
+            const bool present = tbl[(static_cast<uint32_t>(i) * inv_tpb) >> 16] >= 0;
             unsigned char* kt = ring + st * C::STAGE_BYTES;
             unsigned char* vt = kt + C::TILE_BYTES;
             if (present) {
@@ -421,7 +438,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
                 }
                 if (mx0 > m0 + kLazyRescale) {
-                    const float a0 = exp2f(m0 - mx0);
+                    const float a0 = ex2_approx(m0 - mx0);
                     l0 *= a0;
 #pragma unroll
                     for (int mt = 0; mt < KSTEPS; ++mt) {
@@ -431,7 +448,7 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                     m0 = mx0;
                 }
                 if (mx1 > m1 + kLazyRescale) {
-                    const float a1 = exp2f(m1 - mx1);
+                    const float a1 = ex2_approx(m1 - mx1);
                     l1 *= a1;
 #pragma unroll
                     for (int mt = 0; mt < KSTEPS; ++mt) {
@@ -440,8 +457,8 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
                     }
                     m1 = mx1;
                 }
-                const float p0 = exp2f(sc[0] - m0), p1 = exp2f(sc[1] - m1);
-                const float p2 = exp2f(sc[2] - m0), p3 = exp2f(sc[3] - m1);
+                const float p0 = ex2_approx(sc[0] - m0), p1 = ex2_approx(sc[1] - m1);
+                const float p2 = ex2_approx(sc[2] - m0), p3 = ex2_approx(sc[3] - m1);
                 l0 += p0 + p2;
                 l1 += p1 + p3;
                 // P^T operand: transpose the 8x8 (token x head) halves
