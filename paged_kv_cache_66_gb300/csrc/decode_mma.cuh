@@ -426,16 +426,21 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
                 // sc = {S[tok g][h0], S[tok g][h1], S[tok g+8][h0], S[tok g+8][h1]}
-                const bool v0 = g < nv, v1 = g + 8 < nv;
-                sc[0] = v0 ? sc[0] * sl2 : -INFINITY;
-                sc[1] = v0 ? sc[1] * sl2 : -INFINITY;
-                sc[2] = v1 ? sc[2] * sl2 : -INFINITY;
-                sc[3] = v1 ? sc[3] * sl2 : -INFINITY;
-                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                for (int e = 0; e < 4; ++e) sc[e] *= sl2;
+                if (nv < C::TILE) {  // the partition's last tile only
+                    if (g >= nv) sc[0] = sc[1] = -INFINITY;
+                    if (g + 8 >= nv) sc[2] = sc[3] = -INFINITY;
+                }
+                float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+                // A head's max moves only when one of its 8 token lanes passes the lazy threshold;
+                // one vote finds the (rare) tiles where some head's does, and only those reduce.
+                if (__any_sync(0xffffffffu, mx0 > m0 + kLazyRescale || mx1 > m1 + kLazyRescale)) {
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
                 }
                 if (mx0 > m0 + kLazyRescale) {
                     const float a0 = ex2_approx(m0 - mx0);
