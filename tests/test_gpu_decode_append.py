@@ -102,6 +102,8 @@ CASES = [
     (16, 2, 256, 16, [1, 200, 900], 0),
     (32, 8, 128, 256, [1, 255, 256, 257, 1500], 0),
     (16, 4, 64, 16, [0, 300, 0, 1025], 0),                   # empty sequences (slot -1)
+    (32, 8, 128, 48, [1, 48, 49, 700], 480),                 # three 16-token tiles per block
+    (8, 2, 128, 240, [1, 240, 241, 1500], 480),              # fifteen tiles per block
 ]
 
 

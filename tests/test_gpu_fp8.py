@@ -110,6 +110,8 @@ FP8_CASES = [
     (16, 4, 64, 16, [1, 15, 17, 511, 513, 1300], 0),     # D = 64: two 64-byte rows per swizzled line
     (8, 1, 64, 32, [40, 700], 64),
     (32, 4, 64, 16, [3, 300], 0),                        # G = 8
+    (32, 8, 128, 48, [47, 49, 1000], 480),               # three 16-token tiles per block
+    (16, 4, 64, 80, [79, 81, 900], 400),                 # five tiles per block, token-pair lines
 ]
 
 

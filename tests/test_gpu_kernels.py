@@ -161,6 +161,11 @@ CASES = [
     (8, 1, 128, 64, [1, 65, 900], 0),                   # MQA, b = 64
     (32, 8, 128, 256, [1, 255, 256, 257, 1500], 0),     # b = 256: one block per half partition
     (16, 4, 64, 128, [300, 1025], 0),
+    # blocks of 3, 5, 6 and 15 tiles of 16 tokens: a tile finds its table entry by division
+    (32, 8, 128, 48, [1, 47, 48, 49, 700, 1441], 480),
+    (16, 4, 64, 80, [1, 79, 81, 1000], 400),
+    (16, 2, 256, 96, [95, 97, 800], 480),
+    (8, 2, 128, 240, [1, 239, 241, 1500], 480),
 ]
 
 
