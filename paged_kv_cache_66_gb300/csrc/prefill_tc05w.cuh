@@ -6,8 +6,11 @@
 // One CTA owns 256 query rows of one KV head as two 128-row tiles X = A, B that
 // share every 128-key K/V tile j.  Tensor memory holds O_A, O_B and one S buffer
 // per tile (2 D + 2 x 128 columns); P_Xj (two 16-bit values per column) overwrites
-// the first 64 columns of S_X.  The MMA issuer keeps one fixed order:
-//   O_A += P_Aj V_j,  S_A(j+1) = Q_A K_(j+1)^T,  O_B += P_Bj V_j,  S_B(j+1) = Q_B K_(j+1)^T
+// the first 64 columns of S_X.  P_Xj is published in two halves (keys 0-31 and 64-95,
+// then 32-63 and 96-127: each softmax thread's first and second 32 keys), and the
+// P . V k-steps of the first half start while the second is computed.  The MMA
+// issuer keeps one fixed order:
+//   O_A += P_Aj V_j (two halves),  S_A(j+1) = Q_A K_(j+1)^T,  O_B += P_Bj V_j,  S_B(j+1) = Q_B K_(j+1)^T
 // so the softmax of one tile overlaps the other tile's MMAs.  S_X(j+1) follows
 // P_Xj . V_j on the tensor pipe, which performs one thread's MMAs in issue order;
 // and the commit that reports S_X(j+1) done reports every earlier MMA of the
@@ -71,8 +74,8 @@ struct Tc05wCfg {
     static constexpr int K_OFF = Q_BYTES;
     static constexpr int V_OFF = K_OFF + SLOTS * SLOT_BYTES;
     static constexpr int BAR_OFF = V_OFF + SLOTS * SLOT_BYTES;
-    // k_full, k_empty, v_full, v_empty [SLOTS]; s_full, p_full [2]; o_final; q_full
-    static constexpr int NBARS = 4 * SLOTS + 4 + 2;
+    // k_full, k_empty, v_full, v_empty [SLOTS]; s_full [2]; p_full [2][2] (tile, half); o_final; q_full
+    static constexpr int NBARS = 4 * SLOTS + 6 + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int RED_OFF = MISC_OFF + 64;  // row max exchange [2][2][2][128], row sums [2][2][128]
     static constexpr size_t smem_bytes = 1024 + RED_OFF + (8 + 4) * 128 * 4;
@@ -100,8 +103,8 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
     uint64_t* v_full = k_empty + SLOTS;
     uint64_t* v_empty = v_full + SLOTS;
     uint64_t* s_full = v_empty + SLOTS;  // [X]
-    uint64_t* p_full = s_full + 2;       // [X]
-    uint64_t* o_final = p_full + 2;
+    uint64_t* p_full = s_full + 2;       // [X][half]: keys 32 q .. of each 64-key half, q = half
+    uint64_t* o_final = p_full + 4;
     uint64_t* q_full = o_final + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
     int* slot_ok = reinterpret_cast<int*>(smem + C::MISC_OFF + 16);  // loaded sub-tiles of each V slot (bit mask)
@@ -134,7 +137,8 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
 #pragma unroll
         for (int X = 0; X < 2; ++X) {
             mbar_init(&s_full[X], 1);
-            mbar_init(&p_full[X], 256);
+            mbar_init(&p_full[X * 2], 256);
+            mbar_init(&p_full[X * 2 + 1], 256);
         }
         mbar_init(o_final, 1);
         mbar_init(q_full, C::NSW * 32);
@@ -229,13 +233,15 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                 // reports S_X(j) and every earlier MMA of this thread (P_X(j-1) . V_(j-1) included) done
                 tc05::commit(&s_full[X]);
             };
-            auto issue_pv = [&](int X, int j) {
+            // the k-steps of half q of P_Xj: keys 32 q .. 32 q + 31 and 64 + 32 q .. (k-steps 2q, 2q+1, 4+2q, 5+2q)
+            auto issue_pv = [&](int X, int j, int q) {
                 const uint64_t vst = v_desc + static_cast<uint64_t>((j % SLOTS) * (C::SLOT_BYTES >> 4));
                 const uint32_t pa = tmem + C::S_COL + X * BN;  // key k at column k / 2
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
+                for (int i = 0; i < BN / 32; ++i) {
+                    const int kk = (i >> 1) * 4 + 2 * q + (i & 1);
                     const uint64_t b = vst + static_cast<uint64_t>((kk * 2048) >> 4);
-                    tc05::mma_ts(tmem + C::O_COL + X * D, pa + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc05::mma_ts(tmem + C::O_COL + X * D, pa + kk * 8, b, ID_PV, (j > 0 || q > 0 || i > 0) ? 1u : 0u);
                 }
             };
             // k_full / v_full of tile j cannot complete the next phase of their slot before k_empty /
@@ -253,21 +259,30 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                 const int sl = j % SLOTS;
                 const bool more = j + 1 < n_kv;
                 ok = mbar_wait_bounded(&v_full[sl], (j / SLOTS) & 1);
-                // P_X(j+1) needs S_X(j+1), issued below after this wait: p_full is at most one phase ahead
+                // P_X(j+1) needs S_X(j+1), issued below after both waits of P_Xj: each half's
+                // p_full is at most one phase ahead
                 ok = ok && mbar_wait_bounded(&p_full[0], j & 1);
                 if (!ok) break;
                 tc05::fence_after();
-                issue_pv(0, j);
+                issue_pv(0, j, 0);
+                ok = mbar_wait_bounded(&p_full[1], j & 1);
+                if (!ok) break;
+                tc05::fence_after();
+                issue_pv(0, j, 1);
                 if (more) {
                     ok = mbar_wait_bounded(&k_full[(j + 1) % SLOTS], ((j + 1) / SLOTS) & 1);
                     if (!ok) break;
                     tc05::fence_after();
                     issue_s(0, j + 1);  // after P_A(j) . V_j on the pipe: overwrites P_A(j) in S_A
                 }
-                ok = mbar_wait_bounded(&p_full[1], j & 1);
+                ok = mbar_wait_bounded(&p_full[2], j & 1);
                 if (!ok) break;
                 tc05::fence_after();
-                issue_pv(1, j);
+                issue_pv(1, j, 0);
+                ok = mbar_wait_bounded(&p_full[3], j & 1);
+                if (!ok) break;
+                tc05::fence_after();
+                issue_pv(1, j, 1);
                 tc05::commit(&v_empty[sl]);  // V_j is free once both P . V_j complete
                 if (more) {
                     issue_s(1, j + 1);
@@ -396,6 +411,19 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
         }
         const float ms = m == -INFINITY ? 0.f : m;
         const float mul = interior ? sl2 : 1.f;
+        // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero them
+        // before the first half of P is published (both groups write the same zeros; each
+        // P . V waits only for its own group's)
+        if (key0 + BN > L || okmask != (1 << SUB) - 1) {
+            unsigned char* vt = smem + C::V_OFF + sl * C::SLOT_BYTES;
+            for (int e = hh * 128 + r; e < BN * NBOX * 8; e += 256) {
+                const int key = e / (NBOX * 8), rest = e % (NBOX * 8);
+                if (key0 + key >= L || !((okmask >> (key >> 4)) & 1))
+                    *reinterpret_cast<uint4*>(vt + (rest >> 3) * C::KV_BOX + key * 128 + (rest & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+        }
         // ---- P = 2^(v * mul - m): keys 64 hh + 32 q .. +31 go to columns 32 hh + 16 q .. +15
         // (two 16-bit values per column), over scores already in registers
         // (pairs of keys in packed fp32 FMAs and adds: the softmax is issue-bound here)
@@ -413,23 +441,11 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                 pw[i] = pack2<T>(e0, e1);
             }
             tc05::st16(sa + hh * 32 + qq * 16, pw);
+            tc05::wait_st();
+            tc05::fence_before();
+            mbar_arrive(&p_full[X * 2 + qq]);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero them
-        // (both groups write the same zeros; each P . V waits only for its own group's)
-        if (key0 + BN > L || okmask != (1 << SUB) - 1) {
-            unsigned char* vt = smem + C::V_OFF + sl * C::SLOT_BYTES;
-            for (int e = hh * 128 + r; e < BN * NBOX * 8; e += 256) {
-                const int key = e / (NBOX * 8), rest = e % (NBOX * 8);
-                if (key0 + key >= L || !((okmask >> (key >> 4)) & 1))
-                    *reinterpret_cast<uint4*>(vt + (rest >> 3) * C::KV_BOX + key * 128 + (rest & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-        }
-        tc05::wait_st();
-        tc05::fence_before();
-        mbar_arrive(&p_full[X]);
     }
     griddep_launch_dependents();
     const bool all_ok = tc05::bar_and(2, C::NSW * 32, ok);
