@@ -338,3 +338,19 @@ def test_host_replay_matches_oracle_bit_exact(make):
     for g, w in zip(got, want):
         for key in g:
             assert g[key] == [tuple(x) for x in w[key]] if key == "pairs" else g[key] == w[key], key
+
+
+def test_decode_tile_to_table_entry_is_exact_over_the_accepted_shapes():
+    """The tensor-core decode finds tile i's table entry as (i * ceil(65536 / t)) >> 16 with
+    t = b / 16 tiles per block, instead of dividing.  The limits the C ABI accepts (partition
+    tokens, block size) bound i and t; the quotient must be exact over all of them."""
+    api_src = open(os.path.join(ROOT, "paged_kv_cache_66_gb300", "csrc", "pa_api.cu")).read()
+    kern_src = open(os.path.join(ROOT, "paged_kv_cache_66_gb300", "csrc", "decode_mma.cuh")).read()
+    max_part = int(re.search(r"constexpr int kMaxPartition = (\d+);", api_src).group(1))
+    max_b = int(re.search(r"block_size % 16 != 0 \|\| block_size > (\d+)\) return PA_ERR_UNSUPPORTED", api_src).group(1))
+    assert "(65536u + tpb - 1) / tpb" in kern_src and "* inv_tpb) >> 16" in kern_src
+    i = np.arange(max_part // 16, dtype=np.uint64)
+    for t in range(1, max_b // 16 + 1):
+        inv = (65536 + t - 1) // t
+        assert np.array_equal((i * np.uint64(inv)) >> np.uint64(16), i // np.uint64(t)), t
+        assert int(i[-1]) * inv < 2**32  # the product stays within the kernel's 32-bit unsigned
