@@ -1,6 +1,5 @@
 """The seeded input generator and the oracle's op replay (CPU only)."""
 import numpy as np
-import pytest
 import torch
 
 from oracle import attention, driver
