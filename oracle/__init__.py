@@ -13,8 +13,9 @@ Sources restated here (cited by page title and section):
   [P5] "Chapter 7 Paged KV Cache and Memory Management" (zero-to-sglang)
 
 Modules:
-  blocks     -- BlockAllocator, SeqTables, PrefixTable            ([P1] allocator,
-                paged cache, prefix caching; readings noted per function)
+  blocks     -- BlockAllocator, SeqTables, KeyedPrefixIndex / PrefixTable
+                ([P1] allocator, paged cache, prefix caching; written from the
+                invariants the pages fix, readings in the module header)
   cache_ops  -- K/V scatter through slots and block copy-on-write ([P1] update/reserve)
   attention  -- decode attention by its definition (fp64), the blockwise
                 online-softmax / split merge used only as a cross-check ([P5] 4.2)

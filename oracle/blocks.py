@@ -1,21 +1,30 @@
-"""Host bookkeeping of the paged KV cache, restated from the pages.
+"""Host bookkeeping of the paged KV cache: pool, block tables, prefix index.
 
-[P1] "25. Paged attention and prefix caching", sections "Paging", "The
-allocator", "The paged cache", "Sharing blocks: forks and copy-on-write",
-"Prefix caching".
+TEST INFRASTRUCTURE (oracle): restated from [P1] "25. Paged attention and
+prefix caching", sections "Paging", "The allocator", "The paged cache",
+"Sharing blocks: forks and copy-on-write" and "Prefix caching".  What the
+pages fix, and what every structure below keeps true after each operation:
+
+  * Pool: every physical block is either free (holder count 0, on the free
+    queue exactly once) or live (count = number of block-table entries plus
+    prefix-index entries that hold it).  free + live = N at all times.
+  * A sequence of L tokens holds ceil(L / b) blocks; logical position p lives
+    in the table's entry p // b at offset p % b ("Paging").
+  * A block with more than one holder is never written: before tokens land in
+    it, the writer gets a private copy (copy-on-write, "Sharing blocks").
+  * The prefix index maps the key of a full block's prefix to the block; it
+    holds a reference of its own, and reclaims least-recently-used entries
+    whose block no sequence holds ("Prefix caching").
 
 Readings where the pages differ or are silent:
-  * free-list order: first-in first-out, as in [P1] "The allocator" (a deque
-    popped at the front, released blocks appended at the back), seeded with a
-    caller-given initial order.  ([P2] "Код" pops the end of a list instead.)
-  * over-release: checked before the decrement; raises RuntimeError and leaves
-    the state unchanged ([P2] "Код" asserts before decrementing; [P1] would
-    leave the count at -1).
-  * sharing a block that is not live (refcount 0) raises RuntimeError.
-  * allocation failure inside ``reserve`` is all-or-nothing: the number of
-    fresh blocks is counted first and MemoryError is raised before any state
-    changes ([P1] raises from inside the loop).
-  * no zeroing of a block on allocation ([P2] zeroes; [P1] does not).
+  * free-queue order: first-in first-out ([P1] "The allocator"), seeded with
+    a caller-given initial order ([P2] "Код" takes the end of a list instead);
+  * over-release: checked before the count changes; RuntimeError, state
+    unchanged ([P2] "Код"; [P1] would leave the count at -1);
+  * sharing a free block (count 0) is a caller bug: RuntimeError;
+  * a reservation that cannot be met raises MemoryError before any state
+    changes (all-or-nothing; [P1] raises part-way through);
+  * no zeroing of a block when it is handed out ([P2] zeroes; [P1] does not).
 """
 from __future__ import annotations
 
@@ -23,177 +32,209 @@ from collections import OrderedDict, deque
 
 
 class BlockAllocator:
-    """Free list plus per-block reference counts ([P1] "The allocator")."""
+    """N physical blocks: a FIFO queue of the free ones and a holder count per block."""
 
     def __init__(self, num_blocks: int, order=None):
-        self.num_blocks = int(num_blocks)
-        start = range(self.num_blocks) if order is None else [int(x) for x in order]
-        if sorted(start) != list(range(self.num_blocks)):
+        n = int(num_blocks)
+        first_free = list(range(n)) if order is None else [int(x) for x in order]
+        if sorted(first_free) != list(range(n)):
             raise ValueError("initial order must be a permutation of the pool")
-        self.free = deque(start)
-        self.refs = [0] * self.num_blocks
+        self.num_blocks = n
+        self.refs = [0] * n             # holder count per block; 0 <=> on the free queue
+        self.free = deque(first_free)   # the block free the longest is at the left
+
+    @property
+    def num_free(self) -> int:
+        return len(self.free)
+
+    def _require_live(self, block: int, what: str) -> None:
+        if self.refs[block] < 1:
+            raise RuntimeError(f"{what}: block {block} has no holder")
 
     def allocate(self) -> int:
-        if not self.free:
+        """Hand out the block that has been free the longest, with one holder."""
+        if len(self.free) == 0:
             raise MemoryError("KV block pool exhausted")
         block = self.free.popleft()
         self.refs[block] = 1
         return block
 
     def share(self, block: int) -> None:
-        if self.refs[block] <= 0:
-            raise RuntimeError(f"block {block} is not live")
-        self.refs[block] += 1
+        """One more holder of a live block."""
+        self._require_live(block, "share")
+        self.refs[block] = self.refs[block] + 1
 
     def release(self, block: int) -> None:
-        if self.refs[block] <= 0:
-            raise RuntimeError(f"block {block} released more times than it was referenced")
-        self.refs[block] -= 1
-        if self.refs[block] == 0:
+        """One holder fewer; the last one returns the block to the back of the queue."""
+        self._require_live(block, "release (more releases than references)")
+        left = self.refs[block] - 1
+        self.refs[block] = left
+        if left == 0:
             self.free.append(block)
-
-    @property
-    def num_free(self) -> int:
-        return len(self.free)
 
 
 class SeqTables:
-    """Per-sequence block tables and lengths over one allocator.
+    """Block table and length of every live sequence, over one pool.
 
-    [P1] "The paged cache" (create, blocks_needed, reserve, set_batch, fork,
-    free, truncate) without the tensors: copy-on-write returns the (source,
-    destination) block pairs that the device must copy in every layer.
+    Copy-on-write is reported, not performed: ``reserve`` returns the (source,
+    destination) block pairs the device must copy in every layer's K and V
+    pools before it writes.
     """
 
     def __init__(self, num_blocks: int, block_size: int, order=None):
         self.allocator = BlockAllocator(num_blocks, order)
         self.block_size = int(block_size)
-        self.tables: dict = {}
-        self.lengths: dict = {}
+        self.tables: dict = {}     # sequence id -> list of physical blocks
+        self.lengths: dict = {}    # sequence id -> tokens written
 
-    # [P1] "Paging": a sequence of L tokens needs ceil(L / b) blocks.
     def blocks_needed(self, tokens: int) -> int:
-        return -(-int(tokens) // self.block_size)
+        """ceil(tokens / b): the blocks that hold ``tokens`` tokens ([P1] "Paging")."""
+        q, r = divmod(int(tokens), self.block_size)
+        return q + (1 if r else 0)
 
     def create(self, seq) -> None:
         if seq in self.tables:
             raise ValueError(f"sequence {seq} already exists")
-        self.tables[seq] = []
-        self.lengths[seq] = 0
+        self.tables[seq], self.lengths[seq] = [], 0
 
     def reserve(self, seq, new_tokens: int) -> list:
-        """Make blocks exist for positions [length, length + new_tokens).
+        """Make positions [length, length + new_tokens) writable by ``seq``.
 
-        A table entry in the written range whose block is shared (refcount > 1)
-        is replaced by a fresh block: allocate, record the copy, release the old
-        block, repoint ([P1] "The paged cache", reserve; "Sharing blocks").
+        Two kinds of table entries are touched, in this order ([P1] "The paged
+        cache", reserve): existing entries of the written range whose block
+        has another holder each get a fresh block (take a fresh block, record
+        the copy, drop this sequence's hold on the old one, repoint); then
+        fresh blocks are appended until the table covers the range.  The
+        whole demand is counted first, so a failure changes nothing.
         """
-        table, start = self.tables[seq], self.lengths[seq]
-        end = start + int(new_tokens)
-        need = self.blocks_needed(end)
-        first = start // self.block_size
-        cow = [i for i in range(first, min(len(table), need))
-               if self.allocator.refs[table[i]] > 1]
-        grow = max(0, need - len(table))
-        if len(cow) + grow > self.allocator.num_free:
+        table = self.tables[seq]
+        length = self.lengths[seq]
+        covered = self.blocks_needed(length + int(new_tokens))
+        written = range(length // self.block_size, min(covered, len(table)))
+        refs = self.allocator.refs
+        shared = [i for i in written if refs[table[i]] > 1]
+        appended = max(0, covered - len(table))
+        if len(shared) + appended > self.allocator.num_free:
             raise MemoryError("KV block pool exhausted")
-        pairs = []
-        for i in range(first, min(len(table), need)):
-            old = table[i]
-            if self.allocator.refs[old] > 1:          # shared: copy before writing
-                fresh = self.allocator.allocate()
-                pairs.append((old, fresh))
-                self.allocator.release(old)
-                table[i] = fresh
-        while len(table) < need:
-            table.append(self.allocator.allocate())
-        return pairs
+        copies = []
+        for i in shared:
+            old, fresh = table[i], self.allocator.allocate()
+            copies.append((old, fresh))
+            self.allocator.release(old)
+            table[i] = fresh
+        table.extend(self.allocator.allocate() for _ in range(appended))
+        return copies
 
     def slot(self, seq, pos: int) -> int:
-        """Slot of logical position ``pos``: physical block table[pos // b] at
-        offset pos % b ([P1] "Paging"), encoded as block * b + offset."""
-        table = self.tables[seq]
-        return table[pos // self.block_size] * self.block_size + pos % self.block_size
+        """Slot of logical position ``pos``: offset pos % b of block table[pos // b]
+        ([P1] "Paging"), encoded as block * b + offset."""
+        entry, offset = divmod(int(pos), self.block_size)
+        return self.tables[seq][entry] * self.block_size + offset
 
     def advance(self, seq, n: int) -> None:
-        """Commit ``n`` written tokens ([P1] update: length = last position + 1)."""
-        self.lengths[seq] += int(n)
+        """Count ``n`` more written tokens ([P1] update: length = last position + 1)."""
+        self.lengths[seq] = self.lengths[seq] + int(n)
 
     def fork(self, parent, child) -> None:
-        """Child aliases the parent's blocks ([P1] "Sharing blocks")."""
+        """``child`` starts as an alias of every block of ``parent`` ([P1] "Sharing blocks")."""
         self.create(child)
-        self.tables[child] = list(self.tables[parent])
-        self.lengths[child] = self.lengths[parent]
-        for block in self.tables[child]:
+        inherited = list(self.tables[parent])
+        for block in inherited:
             self.allocator.share(block)
-
-    def free(self, seq) -> None:
-        for block in self.tables.pop(seq):
-            self.allocator.release(block)
-        self.lengths.pop(seq)
+        self.tables[child] = inherited
+        self.lengths[child] = self.lengths[parent]
 
     def truncate(self, seq, length: int) -> None:
+        """Keep the first ``length`` tokens; blocks past them lose this holder, in table order."""
+        table = self.tables[seq]
         keep = self.blocks_needed(length)
-        for block in self.tables[seq][keep:]:
+        dropped = table[keep:]
+        del table[keep:]
+        for block in dropped:
             self.allocator.release(block)
-        del self.tables[seq][keep:]
         self.lengths[seq] = int(length)
 
+    def free(self, seq) -> None:
+        """Drop the sequence: every block it holds loses this holder, in table order."""
+        self.truncate(seq, 0)
+        del self.tables[seq], self.lengths[seq]
+
     def batch(self, seqs):
-        """Block-table rows padded with 0 to the longest table, and lengths
-        ([P1] set_batch)."""
+        """Rows of the device block table (padded with block 0 to the widest row)
+        and the lengths, for ``seqs`` in order ([P1] set_batch)."""
         seqs = list(seqs)
-        width = max([len(self.tables[s]) for s in seqs] + [1])
-        rows = [self.tables[s] + [0] * (width - len(self.tables[s])) for s in seqs]
+        width = max([1] + [len(self.tables[s]) for s in seqs])
+        rows = [list(self.tables[s]) + [0] * (width - len(self.tables[s])) for s in seqs]
         return rows, [self.lengths[s] for s in seqs]
 
 
-class PrefixTable:
-    """Prefix cache that only edits block tables and refcounts ([P1] "Prefix caching").
+class KeyedPrefixIndex:
+    """Prefix index over one SeqTables, generic in how a full block's key is formed.
 
-    Keys are whole token prefixes up to the end of a full block; the cache holds
-    its own reference on each cached block; eviction is least-recently-used
-    among entries nobody else uses.
+    ``block_keys(tokens, salt)`` yields the keys of the full blocks of
+    ``tokens`` in order; key i must identify tokens[: (i + 1) * b] (and the
+    salt).  ``entries`` maps key -> block, least recently used first.
     """
 
     def __init__(self, tables: SeqTables):
         self.tables = tables
         self.entries: OrderedDict = OrderedDict()
 
-    def attach(self, seq, prompt) -> int:
-        t = self.tables
-        t.create(seq)
-        size, reused = t.block_size, 0
-        prompt = list(prompt)
-        # at least one prompt token is always left to prefill
-        while reused + size <= len(prompt) - 1:
-            key = tuple(prompt[:reused + size])
-            block = self.entries.get(key)
-            if block is None:
-                break
-            self.entries.move_to_end(key)
-            t.allocator.share(block)
-            t.tables[seq].append(block)
-            reused += size
-        t.lengths[seq] = reused
-        return reused
+    def block_keys(self, tokens, salt):
+        raise NotImplementedError
 
-    def remember(self, seq, tokens) -> None:
-        t = self.tables
-        tokens = list(tokens)
-        for index in range(len(tokens) // t.block_size):
-            key = tuple(tokens[:(index + 1) * t.block_size])
-            if key not in self.entries:
-                block = t.tables[seq][index]
-                t.allocator.share(block)
-                self.entries[key] = block
+    def attach(self, seq, prompt, salt: bytes = b"") -> int:
+        """Create ``seq`` holding the longest run of cached full blocks that
+        starts the prompt, leaving at least one prompt token to prefill (its
+        logits are needed).  Returns the tokens reused."""
+        prompt = list(prompt)
+        b = self.tables.block_size
+        usable = max(0, (len(prompt) - 1) // b)   # full blocks that leave a token over
+        hits = []
+        for i, key in enumerate(self.block_keys(prompt, salt)):
+            if i == usable or key not in self.entries:
+                break
+            hits.append(key)
+        self.tables.create(seq)
+        held = []
+        for key in hits:
+            self.entries.move_to_end(key)          # most recently used now
+            block = self.entries[key]
+            self.tables.allocator.share(block)
+            held.append(block)
+        self.tables.tables[seq] = held
+        self.tables.lengths[seq] = len(held) * b
+        return len(held) * b
+
+    def remember(self, seq, tokens, salt: bytes = b"") -> None:
+        """Publish the full blocks of ``seq`` (which holds ``tokens``) whose key
+        is not cached yet; the index takes its own reference on each."""
+        table = self.tables.tables[seq]
+        for i, key in enumerate(self.block_keys(list(tokens), salt)):
+            if key in self.entries:
+                continue
+            self.tables.allocator.share(table[i])
+            self.entries[key] = table[i]
 
     def evict(self, blocks_wanted: int) -> None:
-        t = self.tables
-        for key in list(self.entries):
-            if t.allocator.num_free >= blocks_wanted:
-                break
-            block = self.entries[key]
-            if t.allocator.refs[block] == 1:
-                del self.entries[key]
-                t.allocator.release(block)
+        """Free cached blocks, least recently used first, until ``blocks_wanted``
+        blocks are free; only entries whose block has no holder but the index
+        are candidates."""
+        alloc = self.tables.allocator
+        short = int(blocks_wanted) - alloc.num_free
+        if short <= 0:
+            return
+        idle = [key for key, block in self.entries.items() if alloc.refs[block] == 1]
+        for key in idle[:short]:
+            alloc.release(self.entries.pop(key))
+
+
+class PrefixTable(KeyedPrefixIndex):
+    """[P1]'s prefix cache: a block's key is the whole token tuple up to its end."""
+
+    def block_keys(self, tokens, salt):
+        if salt:
+            raise ValueError("token-tuple keys carry no salt")
+        b = self.tables.block_size
+        for end in range(b, len(tokens) + 1, b):
+            yield tuple(tokens[:end])

@@ -17,17 +17,17 @@ Readings (the pages fix no hash function or byte layout):
   * full block i (tokens t[i*b : (i+1)*b]) has the key
         key_i = SHA-256(key_{i-1} || u32le(b) || i64le(t) for each token)
     with key_{-1} = root; a partial last block has no key;
-  * the table built on these keys (HashPrefixTable) has exactly the attach /
-    remember / evict rules of the tuple-keyed PrefixTable, so the two agree
-    step for step whenever no two distinct prefixes share a key.
+  * the table built on these keys (HashPrefixTable) is the generic prefix
+    index of ``blocks`` with this key function: its attach / remember / evict
+    rules are those of the tuple-keyed PrefixTable, so the two agree step for
+    step whenever no two distinct prefixes share a key.
 """
 from __future__ import annotations
 
 import hashlib
 import struct
-from collections import OrderedDict
 
-from .blocks import SeqTables
+from .blocks import KeyedPrefixIndex
 
 DOMAIN = b"pagedkv.prefix.v1"
 
@@ -53,52 +53,18 @@ def chain_keys(tokens, block_size: int, salt: bytes = b"") -> list:
     return keys
 
 
-class HashPrefixTable:
-    """[P1]'s prefix cache with chain keys in place of token tuples.
+class HashPrefixTable(KeyedPrefixIndex):
+    """The prefix index of ``blocks`` with chain keys in place of token tuples.
 
-    attach walks the prompt one full block at a time while the block's chain
-    key is cached, sharing those blocks, and always leaves at least one
-    prompt token to prefill; remember publishes the full blocks of a
-    sequence (the cache takes its own reference); evict drops least-recently
-    used entries whose block nobody else holds until enough blocks are free.
+    Every rule (which blocks attach may reuse, what remember publishes, which
+    entries evict may drop, the LRU order) is the generic index's; only the
+    key differs, so the two tables make the same decisions whenever no two
+    distinct (salt, prefix) pairs share a key.
     """
 
-    def __init__(self, tables: SeqTables):
-        self.tables = tables
-        self.entries: OrderedDict = OrderedDict()
-
-    def attach(self, seq, prompt, salt: bytes = b"") -> int:
-        t = self.tables
-        t.create(seq)
-        size, reused = t.block_size, 0
-        prompt = list(prompt)
+    def block_keys(self, tokens, salt):
         key = root_key(salt)
-        while reused + size <= len(prompt) - 1:
-            key = next_key(key, prompt[reused:reused + size])
-            block = self.entries.get(key)
-            if block is None:
-                break
-            self.entries.move_to_end(key)
-            t.allocator.share(block)
-            t.tables[seq].append(block)
-            reused += size
-        t.lengths[seq] = reused
-        return reused
-
-    def remember(self, seq, tokens, salt: bytes = b"") -> None:
-        t = self.tables
-        for index, key in enumerate(chain_keys(tokens, t.block_size, salt)):
-            if key not in self.entries:
-                block = t.tables[seq][index]
-                t.allocator.share(block)
-                self.entries[key] = block
-
-    def evict(self, blocks_wanted: int) -> None:
-        t = self.tables
-        for key in list(self.entries):
-            if t.allocator.num_free >= blocks_wanted:
-                break
-            block = self.entries[key]
-            if t.allocator.refs[block] == 1:
-                del self.entries[key]
-                t.allocator.release(block)
+        b = self.tables.block_size
+        for start in range(0, len(tokens) - b + 1, b):
+            key = next_key(key, tokens[start:start + b])
+            yield key
