@@ -190,12 +190,19 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
  *   - The first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and caches it; make that
  *     first call before any stream capture.
+ *   - Under CUDA's default lazy module loading, that first lookup is also
+ *     what loads the array onto the device: the driver reserves its
+ *     PA_DECODE_NOALLOC_MAX_BYTES then (with CUDA_MODULE_LOADING=EAGER, when
+ *     the context is created).  So make the first call on each device before
+ *     the application hands all device memory to its own allocator; a first
+ *     call that finds no room returns PA_ERR_CUDA.  Later calls take no
+ *     device memory at all.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind.  Calls whose kernels overlap on the GPU (different streams
  *     without ordering between them) race on it and give wrong results;
  *     serialise them.  No clearing is needed between ordered calls.
- *   - The array stays reserved on every GPU that loads this library's device
- *     code until the process exits.
+ *   - Once loaded, the array stays reserved on that GPU until the process
+ *     exits.
  */
 #define PA_DECODE_NOALLOC_MAX_BYTES (16u << 20)
 pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -327,11 +334,14 @@ pa_status pa_set_prefill_kernel(pa_prefill_kernel kernel);
 
 /*
  * pa_selftest_wait_timeout -- exercise the failure path of the bounded
- * device waits: launch one warp that waits on an mbarrier nothing completes,
- * giving up after `limit_us` microseconds (1..100000).  Afterwards
- * pa_get_device_error reports PA_DEVERR_TIMEOUT (status PA_ERR_TIMEOUT) and
- * the context stays usable.  The decode kernels use the same wait with a
- * 1-second limit.
+ * device waits: launch one warp whose odd lanes wait on an mbarrier that is
+ * completed and whose even lanes wait on one that nothing completes, giving
+ * up after `limit_us` microseconds (1..100000).  As in the decode and prefill
+ * kernels, the warp then takes one decision for all lanes (a vote over the
+ * lanes' own results) before a full-warp shuffle.  Afterwards
+ * pa_get_device_error reports PA_DEVERR_TIMEOUT (status PA_ERR_TIMEOUT) --
+ * set only when the vote failed and the shuffle saw every lane -- and the
+ * context stays usable.  The kernels use the same wait with a 1-second limit.
  */
 pa_status pa_selftest_wait_timeout(int limit_us, void* stream);
 

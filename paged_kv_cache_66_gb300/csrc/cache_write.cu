@@ -202,18 +202,35 @@ cudaError_t launch_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype
     return cudaSuccess;
 }
 
-// Failure-path check of the bounded waits: one warp initialises an mbarrier
-// that nothing will ever complete and waits on it with the same helper the
-// decode kernels use, for at most `limit_ns`.  The wait gives up, the kernel
-// records PA_DEVERR_TIMEOUT and returns; nothing hangs and nothing faults.
+// Failure-path check of the bounded waits, in the shape the decode and
+// prefill kernels use them: each lane of one warp waits, for at most
+// `limit_ns`, on one of two mbarriers -- odd lanes on one whose phase 0 is
+// completed here, even lanes on one that nothing completes -- so the lanes'
+// own results differ.  The warp then decides together (__all_sync) and runs a
+// full-mask shuffle reduction, as the kernels do after their waits.  Lane 0
+// records PA_DEVERR_TIMEOUT only if the vote failed and the reduction saw all
+// 32 lanes with the expected split (16 waits met, 16 given up); nothing hangs
+// and nothing faults.
 __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, int* err) {
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar[2];
+    const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
         fence_mbar_init();
     }
     __syncwarp();
-    if (!mbar_wait_bounded(&bar, 0, limit_ns) && threadIdx.x == 0) flag_error(err, PA_DEVERR_TIMEOUT);
+    if (threadIdx.x == 0) mbar_arrive(&bar[1]);  // completes phase 0 of bar[1]; bar[0] stays open
+    __syncwarp();
+    const bool mine = mbar_wait_bounded(&bar[lane & 1], 0, limit_ns);
+    const bool all_ok = __all_sync(0xffffffffu, mine);
+    int met = mine ? 1 : 0, present = 1;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        met += __shfl_xor_sync(0xffffffffu, met, o);
+        present += __shfl_xor_sync(0xffffffffu, present, o);
+    }
+    if (lane == 0 && !all_ok && met == 16 && present == 32) flag_error(err, PA_DEVERR_TIMEOUT);
 }
 
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream) {

@@ -384,9 +384,12 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         for (int j = 0; j < my_n && !aborted; ++j) {
             const int jj = u * my_n + j;
             const int st = jj % STAGES;
-            if (!mbar_wait_bounded(&bars[st], (jj / STAGES) & 1)) {
+            // the warp decides together: ldmatrix / mma / shuffles below are full-warp collectives,
+            // so a lane whose own wait ran out must not leave the others behind
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], (jj / STAGES) & 1))) {
                 if (lane == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
-                for (int r = jj + 1; r < my_total && r < jj + STAGES; ++r)
+                // let every copy this warp issued land before the CTA may exit (bounded again)
+                for (int r = jj; r < my_total && r < jj + STAGES; ++r)
                     mbar_wait_bounded(&bars[r % STAGES], (r / STAGES) & 1);
                 aborted = true;
                 break;

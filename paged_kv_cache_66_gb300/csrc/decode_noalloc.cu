@@ -10,8 +10,9 @@
 // caller still passes q, the pools, the tables and the output; only the
 // scratch of the partition merge comes from here.
 //
-// The array below is reserved on every GPU on which this library's device
-// code is loaded, and stays reserved until the process exits.
+// The array below is reserved on a GPU when the module holding it is loaded
+// there -- under CUDA's default lazy loading, by the first call's address
+// lookup on that device -- and stays reserved until the process exits.
 #include <cstdint>
 #include <mutex>
 

@@ -164,11 +164,12 @@ __global__ void __launch_bounds__(SimtCfg<T, D, G>::NW * 32)
     bool timed_out = false;
     for (int j = 0; j < my_n; ++j) {
         const int st = j % STAGES;
-        if (!mbar_wait_bounded(&bars[st], (j / STAGES) & 1)) {
+        // one decision for the whole warp: the shuffle reductions below need every lane
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], (j / STAGES) & 1))) {
             timed_out = true;
             if (lane == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
             // let the copies already issued land before the CTA may exit
-            for (int r = j + 1; r < my_n && r < j + STAGES; ++r) mbar_wait_bounded(&bars[r % STAGES], (r / STAGES) & 1);
+            for (int r = j; r < my_n && r < j + STAGES; ++r) mbar_wait_bounded(&bars[r % STAGES], (r / STAGES) & 1);
             break;
         }
         const int i = warp + j * NW;

@@ -51,10 +51,6 @@ struct PrefillCfg {
     static constexpr size_t smem_bytes = 1024 + OK_OFF + STAGES * 4;
 };
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // keeps the 16-bit halves of x (keys k and k + 1) whose key is below nv
 __device__ __forceinline__ uint32_t keep_keys(uint32_t x, int k, int nv) {
     return k + 1 < nv ? x : (k < nv ? (x & 0xFFFFu) : 0u);
@@ -186,7 +182,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::THREADS)
 
     for (int j = 0; j < n_sub; ++j) {
         const int st = j % STAGES;
-        if (!mbar_wait_bounded(&full[st], (j / STAGES) & 1)) {
+        // one decision for the whole warp: ldmatrix, mma and the shuffles below are collectives
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (j / STAGES) & 1))) {
             if (lane == 0) flag_error(p.err, PA_DEVERR_TIMEOUT);
             break;
         }
