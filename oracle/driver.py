@@ -25,10 +25,17 @@ from .blocks import SeqTables
 
 
 class OracleRun:
-    def __init__(self, wl, pools: bool = True, layers=None, kv: str = "native"):
+    def __init__(self, wl, pools: bool = True, layers=None, kv: str = "native", input_device="cpu"):
         """kv = "fp8": the K/V history is what E4M3 pools with the workload's
-        per-(layer, KV head) scales store (content route only)."""
+        per-(layer, KV head) scales store (content route only).
+
+        input_device: where the seeded generator (``workload``) draws the q and
+        K/V values of the content route before they come to the host.  The
+        generator is bit-identical on every device, and all of the oracle's
+        arithmetic runs here in fp64 whatever the choice; a device only makes
+        drawing the long histories of the large workloads fast."""
         self.kv = kv
+        self.input_device = input_device
         if kv == "fp8" and pools:
             raise ValueError("the FP8 replay uses the content route (pools=False)")
         self.wl = wl
@@ -107,7 +114,7 @@ class OracleRun:
         """fp64 outputs [len(rows), Hq, D] for batch rows of a recorded step."""
         wl = self.wl
         rows = list(range(len(rec["uids"]))) if rows is None else list(rows)
-        q = wcfg.q_rows(wl, layer, rec["step"], rows).double().numpy()
+        q = wcfg.q_rows(wl, layer, rec["step"], rows, device=self.input_device).cpu().double().numpy()
         out = np.zeros((len(rows), wl.Hq, wl.D), dtype=np.float64)
         for i, r in enumerate(rows):
             L = int(rec["lens"][r])
@@ -124,8 +131,8 @@ class OracleRun:
         wl = self.wl
         pos = np.arange(length, dtype=np.int64)
         owners = wl.content_owners(uid, pos)
-        K = wcfg.kv_rows(wl, layer, "k", owners, pos)
-        V = wcfg.kv_rows(wl, layer, "v", owners, pos)
+        K = wcfg.kv_rows(wl, layer, "k", owners, pos, device=self.input_device).cpu()
+        V = wcfg.kv_rows(wl, layer, "v", owners, pos, device=self.input_device).cpu()
         if self.kv == "fp8":
             ks, vs = wcfg.kv_scales(wl, layer, "k"), wcfg.kv_scales(wl, layer, "v")
             K = quant.dequantize(quant.quantize_rows(K.float().numpy(), ks), ks, head_axis=1)

@@ -65,13 +65,18 @@ class DeviceStep:
 
 
 class Replay:
-    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None, kv="native", fused=True):
+    def __init__(self, wl, device="cuda", layers=None, partition_tokens=None, kv="native", fused=True,
+                 gen_device=None):
         """kv = "native": pools in the workload's dtype; kv = "fp8": E4M3 pools
         with the workload's per-(layer, KV head) scales.  fused: each layer's
-        newest rows go with its decode in one pa_decode_append (16-bit pools)."""
+        newest rows go with its decode in one pa_decode_append (16-bit pools).
+        gen_device: where the seeded generator draws q and the new K/V rows
+        (default: the pools' device); drawn elsewhere, each tensor is moved to
+        the pools' device in one copy."""
         self.wl = wl
         self.fused = fused and kv == "native" and wl.dtype in ("f16", "bf16")
         self.device = torch.device(device)
+        self.gen_device = self.device if gen_device is None else torch.device(gen_device)
         self.layers = list(range(wl.layers)) if layers is None else list(layers)
         self.host = HostBlockManager(wl.num_blocks, wl.b, wl.free_order)
         self.kv = kv
@@ -177,8 +182,10 @@ class Replay:
         for li, layer in enumerate(self.layers):
             for c0 in range(0, n, chunk):
                 c1 = min(n, c0 + chunk)
-                k = wcfg.kv_rows(wl, layer, "k", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
-                v = wcfg.kv_rows(wl, layer, "v", w.owners[c0:c1], w.positions[c0:c1], device=self.device)
+                k = wcfg.kv_rows(wl, layer, "k", w.owners[c0:c1], w.positions[c0:c1],
+                                 device=self.gen_device).to(self.device)
+                v = wcfg.kv_rows(wl, layer, "v", w.owners[c0:c1], w.positions[c0:c1],
+                                 device=self.gen_device).to(self.device)
                 self.append(li, k, v, slots_d[c0:c1], stream=stream)
 
     def _write(self, uid: int, n: int):
@@ -248,10 +255,11 @@ class Replay:
         all_pairs = np.concatenate([w.pairs.reshape(-1, 2) for w in writes] + [plan.pairs.reshape(-1, 2)])
         rows = np.arange(len(plan.uids))
         q, kn, vn = [], [], []
+        gd = self.gen_device
         for layer in self.layers:
-            q.append(wcfg.q_rows(wl, layer, plan.step, rows, device=dev))
-            kn.append(wcfg.kv_rows(wl, layer, "k", all_owners, all_pos, device=dev))
-            vn.append(wcfg.kv_rows(wl, layer, "v", all_owners, all_pos, device=dev))
+            q.append(wcfg.q_rows(wl, layer, plan.step, rows, device=gd).to(dev))
+            kn.append(wcfg.kv_rows(wl, layer, "k", all_owners, all_pos, device=gd).to(dev))
+            vn.append(wcfg.kv_rows(wl, layer, "v", all_owners, all_pos, device=gd).to(dev))
         d_slots = torch.as_tensor(all_slots).to(dev)
         B = len(plan.uids)
         splits = [self.split_rows(B, k, v, d_slots) for k, v in zip(kn, vn)]
@@ -270,11 +278,16 @@ class Replay:
         wl = self.wl
         B, width = ds.tables.shape
         ws = self.workspace_for(B, width)
+        # one NVTX range per step and per layer (free unless a profiler listens)
+        torch.cuda.nvtx.range_push(f"step {ds.plan.step}")
         if ds.pairs.shape[0]:
             api.pa_copy_blocks(self.k_pools, self.v_pools, ds.pairs, stream=stream)
         if outs is None:
             outs = [torch.empty((B, wl.Hq, wl.D), dtype=wl.torch_dtype, device=self.device) for _ in self.layers]
         for li in range(len(self.layers)):
+            torch.cuda.nvtx.range_push(f"layer {self.layers[li]}")
             self.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables, ds.lens, ws,
                             stream=stream, split=ds.splits[li] if ds.splits else None)
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.nvtx.range_pop()
         return outs

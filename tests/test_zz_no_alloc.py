@@ -3,10 +3,13 @@ device memory (an application that owns all device memory through its own
 allocator, a loop that must not allocate after start-up, an ABI consumer with
 no allocator): its split-K scratch is a fixed array inside the library.
 
-Called through the C ABI and checked against pa_decode with caller-provided
-scratch on two calls in a row with different inputs (the shared array keeps
-the first call's contents), within the fp16 decode tolerance.  Runs alone in a
-fresh process as well as after the rest of the suite.
+Called through the C ABI on two calls in a row with different inputs (the
+shared array keeps the first call's contents).  Each result must equal, bit
+for bit, pa_decode with caller-provided scratch -- the same kernels on the
+same inputs -- and match the fp64 oracle within the fp16 decode tolerance.
+Free device memory must not change across the second call: it allocates
+nothing.  Runs alone in a fresh process as well as after the rest of the
+suite.
 """
 import ctypes as C
 import math
@@ -45,12 +48,15 @@ def _p(t):
 def test_noalloc_decode_matches_caller_scratch_two_calls():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    import numpy as np
+
+    from oracle import attention as oatt
     from paged_kv_cache_66_gb300 import _lib, api
     lib = _lib.load()
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
     cases = [([3000, 700, 1, 4096], 32, 8, 128, 16, 11),     # 8 partitions of 512 tokens
              ([5000, 33, 2048], 16, 2, 256, 32, 12)]          # different shape, more partitions
-    for lengths, Hq, Hkv, D, b, seed in cases:
+    for call, (lengths, Hq, Hkv, D, b, seed) in enumerate(cases):
         q, Kp, Vp, tables, lens = _paged_inputs(lengths, Hq, Hkv, D, b, seed)
         B = len(lengths)
         scale = 1.0 / math.sqrt(D)
@@ -60,12 +66,21 @@ def test_noalloc_decode_matches_caller_scratch_two_calls():
                       workspace=torch.empty(api.pa_decode_workspace_size(B, Hq, D, tables.shape[1], b, 0),
                                             dtype=torch.uint8, device="cuda"))
         out = torch.full_like(q, float("nan"))
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         st = lib.pa_decode_noalloc(_p(out), _p(q), _p(Kp), _p(Vp), Kp.shape[0], _p(tables), tables.shape[1],
                                    _p(lens), B, Hq, Hkv, D, b, scale, 0, F16, stream)
         assert st == 0, lib.pa_status_string(st)
         torch.cuda.synchronize()
-        err = (out.double() - ref.double()).abs().max().item()
-        assert err <= 2e-3, err
+        if call == 1:
+            # the array was set up by the first call; this one must take no device memory
+            assert torch.cuda.mem_get_info()[0] == free_before
+        assert torch.equal(out, ref)
+        Kc, Vc, qc, tc = Kp.cpu(), Vp.cpu(), q.cpu().double().numpy(), tables.cpu().tolist()
+        for s_, L in enumerate(lengths):
+            want = oatt.paged_decode(qc[s_], Kc, Vc, tc[s_], L, b, scale)
+            err = float(np.abs(out[s_].cpu().double().numpy() - want).max())
+            assert err <= 2e-3, (call, s_, err)
     assert api.pa_get_device_error() == 0
 
 
