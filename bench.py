@@ -305,9 +305,165 @@ def cpu_baseline(wl, budget_s: float = 15.0):
 
 # ------------------------------------------------------------------ our arm
 
-def run_ours(args, ws, rank, local):
+def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=True, flush_l2=False,
+                    min_seconds=0.0):
+    """Time ``steps`` decode steps of ``wl`` on the device, inputs resident in HBM.
+
+    The host plans of every step are made and uploaded first.  Without
+    ``flush_l2`` the timed steps run back to back (for histories far larger than
+    L2) and only the decode launches of the last timed steps are bracketed by
+    events (an event between two launches ends their programmatic overlap).
+    With ``flush_l2`` (histories that fit in L2) a 256 MiB write evicts L2
+    before every timed step, each step is bracketed by its own events, and the
+    step time is the sum of those.
+
+    With ``min_seconds`` the ``steps`` planned steps are executed in turn as
+    many times as it takes for the timed region to last about that long (sized
+    by one untimed pass), so that the clock sampler sees the region; executing
+    a planned step again repeats its copies, appends and decode exactly.
+    Returns the Replay (for the e2e leg) and the figures of the run."""
     from paged_kv_cache_66_gb300 import api
     from paged_kv_cache_66_gb300.replay import Replay
+
+    rp = Replay(wl, device=dev, kv=kv, partition_tokens=partition or None, fused=fused)
+    rp.run_setup()
+    torch.cuda.synchronize()
+    total_steps = warmup + steps
+    plans = [rp.plan_step(i) for i in range(total_steps)]
+    dsteps = [rp.device_step(p) for p in plans]
+    outs = [torch.empty((len(plans[0].uids), wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev) for _ in rp.layers]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    # The Python collector is left running: pausing it around the timed regions (gc.disable, with
+    # or without a collection first) halved the host-bound one-layer config-2 step (~30 us of GPU
+    # work per step).
+    for i in range(warmup):
+        rp.run_step(dsteps[i], outs)
+    torch.cuda.synchronize()
+    reps = 1
+    if min_seconds > 0:
+        t0 = time.perf_counter()
+        for j in range(steps):
+            if flush_l2:
+                flush.zero_()
+            rp.run_step(dsteps[warmup + j], outs)
+        torch.cuda.synchronize()
+        reps = max(1, int(np.ceil(min_seconds / max(time.perf_counter() - t0, 1e-6))))
+    order = [warmup + n % steps for n in range(steps * reps)]
+    planned_steps, steps = steps, steps * reps
+    _barrier(ws)
+
+    nL = len(rp.layers)
+    # per-launch events on the decode launches of the last timed steps only (32 launches, or the
+    # last quarter of the steps when fewer): bracketing every launch cost ~2.5 % of the
+    # long-context step and ~30 % of the one-layer, L2-resident step
+    ev_steps = steps if flush_l2 else min(max(1, -(-32 // nL)), max(1, steps // 4))
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(ev_steps * nL)]
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps if flush_l2 else 0)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    t_start.record(stream)
+    for j in range(steps):
+        ds = dsteps[order[j]]
+        B, width = ds.tables.shape
+        wsbuf = rp.workspace_for(B, width)
+        if flush_l2:
+            flush.zero_()
+            ev_step[j][0].record(stream)
+        torch.cuda.nvtx.range_push(f"decode step {j}")
+        if ds.pairs.shape[0]:
+            api.pa_copy_blocks(rp.k_pools, rp.v_pools, ds.pairs)
+            launches += 1
+        for li in range(nL):
+            launches += rp.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables,
+                                      ds.lens, wsbuf,
+                                      events=ev_dec[(j - (steps - ev_steps)) * nL + li]
+                                      if j >= steps - ev_steps else None, split=ds.splits[li])
+            launches += 1 if wsbuf.numel() else 0
+        torch.cuda.nvtx.range_pop()
+        if flush_l2:
+            ev_step[j][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clk = clocks.stop()
+    dev_ms = (sum(a.elapsed_time(b) for a, b in ev_step) if flush_l2 else t_start.elapsed_time(t_end))
+    dev_ms_max = _max_over_ranks(dev_ms, ws, dev)
+    timed = [dsteps[order[j]].plan for j in range(steps)]
+    kv_bytes = sum(_kv_bytes(wl, p.lens, rp.kv_elt) for p in timed) * nL
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    alg = statistics.mean(_alg_bytes_decode(wl, p, rp.kv_elt, rp.fused) for p in timed[steps - ev_steps:])
+    return rp, {
+        "plans": plans, "nL": nL, "B": len(plans[0].uids), "dev_ms_max": dev_ms_max, "kv_bytes": kv_bytes,
+        "steps": steps, "planned_steps": planned_steps,
+        "launches": launches, "clocks": clk, "dec_avg_ms": dec_avg, "dec_med_ms": statistics.median(dec_ms),
+        "alg": alg,
+        "unique": statistics.mean(_unique_kv_bytes(wl, p, rp.kv_elt) for p in timed),
+        "effective": statistics.mean(_kv_bytes(wl, p.lens, rp.kv_elt) for p in timed),
+    }
+
+
+# the other workloads' decode steps, measured in the same run after the headline
+SECONDARY = [
+    {"config": 4, "kv": "native"},
+    {"config": 5, "combo": (128, 4, 16, "bf16"), "kv": "native"},
+    {"config": 5, "combo": (256, 8, 16, "f16"), "kv": "native"},
+    {"config": 5, "combo": (64, 8, 16, "bf16"), "kv": "native"},
+    {"config": 5, "combo": (128, 8, 32, "bf16"), "kv": "native"},
+    {"config": 2, "kv": "native"},
+    {"config": 3, "kv": "fp8"},
+]
+L2_BYTES = 129 << 20
+
+
+def _history_bytes(wl, elt) -> int:
+    """K/V bytes the setup writes (shared tokens once): the history one decode step reads."""
+    tokens = sum(int(op[2]) for op in wl.setup_ops if op[0] == "write")
+    return tokens * 2 * wl.Hkv * wl.D * elt * wl.layers
+
+
+def _secondary(spec, steps, warmup, dev, ws, peak):
+    """One entry of the ``configs`` record: a workload's decode step on its own clock record.
+    A workload whose history is under 4x L2 is timed with L2 flushed before every step."""
+    wl = _workload(spec["config"], warmup + steps + 1, spec.get("combo"))
+    kv = spec["kv"]
+    small = _history_bytes(wl, 1 if kv == "fp8" else wl.elt) < 4 * L2_BYTES
+    rp, m = _measure_device(wl, steps, warmup, dev, ws, kv=kv, flush_l2=small, min_seconds=0.5)
+    steps = m["steps"]
+    ms = m["dev_ms_max"] / steps
+    entry = {
+        "workload": wl.name, "kv_cache": "e4m3" if kv == "fp8" else wl.dtype, "batch": m["B"],
+        "layers": m["nL"], "steps": steps, "planned_steps": m["planned_steps"], "warmup": warmup,
+        "ms_per_step": ms,
+        "effective_kv_gbs": m["kv_bytes"] / (m["dev_ms_max"] / 1e3) / 1e9,
+        "seq_steps_per_s": m["B"] * steps / (m["dev_ms_max"] / 1e3),
+        "kv_bytes_per_decode": {"effective": m["effective"], "unique": m["unique"]},
+        "l2": ("L2 flushed (256 MiB write) before every timed step; each step timed by its own events"
+               if small else "history larger than L2 (no flush needed)"),
+        "roofline": {"bound": "hbm", "peak": peak, "unit": "GB/s",
+                     "alg_bytes_per_launch": m["alg"], "avg_launch_ms": m["dec_avg_ms"],
+                     "median_launch_ms": m["dec_med_ms"],
+                     "achieved": m["alg"] / (m["dec_avg_ms"] / 1e3) / 1e9,
+                     "frac": m["alg"] / (m["dec_avg_ms"] / 1e3) / 1e9 / peak,
+                     "unique_frac": m["unique"] / (m["dec_avg_ms"] / 1e3) / 1e9 / peak,
+                     "step_frac": m["kv_bytes"] / (m["dev_ms_max"] / 1e3) / 1e9 / peak},
+        "clocks": {k: m["clocks"][k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+        "gpu_launches": m["launches"],
+    }
+    if "combo" in spec:
+        entry["combo"] = {"head_dim": wl.D, "group": wl.G, "block_size": wl.b, "dtype": wl.dtype}
+    del rp
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_ours(args, ws, rank, local):
+    from paged_kv_cache_66_gb300 import api
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -317,74 +473,29 @@ def run_ours(args, ws, rank, local):
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
         wl.layers = min(wl.layers, args.layers)
-    rp = Replay(wl, device=dev, kv=args.kv, partition_tokens=args.partition or None, fused=not args.unfused)
-    rp.run_setup()
-    torch.cuda.synchronize()
-
-    # plans of warm-up + timed steps, uploaded before the timed region
-    plans = [rp.plan_step(i) for i in range(total_steps)]
-    dsteps = [rp.device_step(p) for p in plans]
-    outs = [torch.empty((len(plans[0].uids), wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev) for _ in rp.layers]
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    # The Python collector is left running: pausing it around the timed regions (gc.disable, with
-    # or without a collection first) halved the host-bound one-layer config-2 step (~30 us of GPU
-    # work per step).
-    # every timed step reads the whole history (> L2 by far for the long-context workload)
-    for i in range(args.warmup):
-        rp.run_step(dsteps[i], outs)
-    torch.cuda.synchronize()
-    _barrier(ws)
-
-    nL = len(rp.layers)
-    # per-launch events on the launches of the last timed steps only (32 launches, or the last
-    # quarter of the steps when fewer): an event recorded between two launches ends their
-    # programmatic overlap, which cost ~2.5 % of the long-context step when every launch was
-    # bracketed, and ~30 % of the one-layer, L2-resident step
-    ev_steps = min(max(1, -(-32 // nL)), max(1, args.steps // 4))
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(ev_steps * nL)]
-    clocks = ClockSampler(local)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
-    t_start.record(stream)
-    for j in range(args.steps):
-        ds = dsteps[args.warmup + j]
-        B, width = ds.tables.shape
-        wsbuf = rp.workspace_for(B, width)
-        if ds.pairs.shape[0]:
-            api.pa_copy_blocks(rp.k_pools, rp.v_pools, ds.pairs)
-            launches += 1
-        for li in range(nL):
-            launches += rp.step_layer(li, outs[li], ds.q[li], ds.k_new[li], ds.v_new[li], ds.slots, ds.tables,
-                                      ds.lens, wsbuf,
-                                      events=ev_dec[(j - (args.steps - ev_steps)) * nL + li]
-                                      if j >= args.steps - ev_steps else None, split=ds.splits[li])
-            launches += 1 if wsbuf.numel() else 0
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    _barrier(ws)
-    clk = clocks.stop()
-    dev_ms = t_start.elapsed_time(t_end)
-    dev_ms_max = _max_over_ranks(dev_ms, ws, dev)
-    kv = sum(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens, rp.kv_elt) for j in range(args.steps)) * nL
-    kv_all = _sum_over_ranks(float(kv), ws, dev)
+    rp, m = _measure_device(wl, args.steps, args.warmup, dev, ws, kv=args.kv, partition=args.partition,
+                            fused=not args.unfused, flush_l2=args.flush_l2)
+    traffic = _profiled_traffic(_launch_key(args, wl, rp))
+    plans, nL, B = m["plans"], m["nL"], m["B"]
+    dev_ms_max = m["dev_ms_max"]
+    kv_all = _sum_over_ranks(float(m["kv_bytes"]), ws, dev)
     value = kv_all / (dev_ms_max / 1e3) / 1e9
-    B = len(plans[0].uids)
     seq_steps = B * args.steps * ws / (dev_ms_max / 1e3)
-    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
-    dec_avg = sum(dec_ms) / len(dec_ms)
-    dec_med = statistics.median(dec_ms)
-    unique = statistics.mean(_unique_kv_bytes(wl, dsteps[args.warmup + j].plan, rp.kv_elt) for j in range(args.steps))
-    effective = statistics.mean(_kv_bytes(wl, dsteps[args.warmup + j].plan.lens, rp.kv_elt) for j in range(args.steps))
-    alg = statistics.mean(_alg_bytes_decode(wl, dsteps[args.warmup + j].plan, rp.kv_elt, rp.fused)
-                          for j in range(args.steps - ev_steps, args.steps))
+    dec_avg = m["dec_avg_ms"]
     peak, peak_kind = _peaks()
-    achieved = alg / (dec_avg / 1e3) / 1e9
+    achieved = m["alg"] / (dec_avg / 1e3) / 1e9
     err = api.pa_get_device_error()
 
     # ---------------- e2e through the public API with host buffers
     e2e = None if args.no_e2e else run_e2e(args, wl, rp, dev, ws)
+
+    # ---------------- the other workloads (one GPU, headline workload only)
+    configs = None
+    if args.config == 3 and args.kv == "native" and not args.layers and not args.no_configs and ws == 1:
+        del rp
+        torch.cuda.empty_cache()
+        configs = [_secondary(spec, 20, 3, dev, ws, peak) for spec in SECONDARY]
+        err |= api.pa_get_device_error()
 
     if rank != 0:
         return
@@ -395,25 +506,33 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": wl.name, "batch": B, "context": int(np.max(plans[0].lens)), "layers": nL,
                    "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
-                   "partition_tokens": rp.partition_tokens, "kv_cache": "e4m3" if args.kv == "fp8" else wl.dtype,
-                   "l2": "inputs larger than L2 (no flush needed)",
+                   "partition_tokens": wl.partition_tokens if not args.partition else args.partition,
+                   "kv_cache": "e4m3" if args.kv == "fp8" else wl.dtype,
+                   "l2": ("L2 flushed (256 MiB write) before every timed step; each step timed by its own events"
+                          if args.flush_l2 else "inputs larger than L2 (no flush needed)"),
                    "parallelism": f"replicas x{ws}"},
         "seq_steps_per_s": seq_steps,
-        "kv_bytes_per_decode": {"effective": effective, "unique": unique,
-                                "unique_gbs_per_launch": unique / (dec_avg / 1e3) / 1e9},
+        "kv_bytes_per_decode": {"effective": m["effective"], "unique": m["unique"],
+                                "unique_gbs_per_launch": m["unique"] / (dec_avg / 1e3) / 1e9},
         "pct_hbm_peak": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _profiled_traffic(_launch_key(args, wl, rp)),
+                     "frac": achieved / peak, "traffic": traffic,
                      "kernel": (f"pa_decode_append ({args.kernel} partition with the step's append + merge)"
-                                if rp.fused else f"pa_decode ({args.kernel} partition + merge)"),
+                                if not args.unfused and args.kv == "native" and wl.dtype != "f32"
+                                else f"pa_decode ({args.kernel} partition + merge)"),
                      "peak_kind": f"{peak_kind} hbm_gbs",
-                     "alg_bytes_per_launch": alg, "avg_launch_ms": dec_avg, "median_launch_ms": dec_med},
-        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
-                   "samples": clk["samples"]},
+                     "alg_bytes_per_launch": m["alg"], "avg_launch_ms": dec_avg, "median_launch_ms": m["dec_med_ms"],
+                     "launch_timing": ("avg_launch_ms is measured on event-bracketed launches of the last timed "
+                                       "steps; ms_per_step on unbracketed steps, where consecutive launches "
+                                       "overlap their ends, so layers x avg_launch_ms can exceed ms_per_step")},
+        "clocks": {"sm_mhz": m["clocks"]["sm_mhz"], "sm_max_mhz": m["clocks"]["sm_max_mhz"],
+                   "reasons": m["clocks"]["reasons"], "samples": m["clocks"]["samples"]},
         "e2e": e2e,
-        "gpu_launches": launches,
+        "gpu_launches": m["launches"],
         "device_error_word": err,
     }
+    if configs is not None:
+        line["configs"] = configs
     if not args.no_cpu_baseline and ws >= 1 and rank == 0:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
@@ -642,6 +761,9 @@ def main():
     ap.add_argument("--combo", type=str, default="128,4,16,bf16", help="config 5: D,G,b,dtype")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' record")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="evict L2 before every timed step (for workloads whose history fits in L2)")
     ap.add_argument("--layers", type=int, default=0, help="use the first N layers only (profiling)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"], help="decode partition kernel")
     ap.add_argument("--heads-per-cta", type=int, default=0, choices=[0, 1, 2],
