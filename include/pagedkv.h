@@ -113,8 +113,8 @@ pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int num_lay
  * `max_blocks` columns: per (sequence, query head, partition) one running
  * max, one normaliser and D partial output values.  Returns 0 when every
  * sequence fits one partition (max_blocks * b <= partition tokens).
- * partition_tokens = 0 selects the default (512).  The contents need no
- * initialisation.
+ * partition_tokens = 0 selects the automatic size, the same one pa_decode
+ * then uses (see pa_decode).  The contents need no initialisation.
  */
 size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int max_blocks,
                                 int block_size, int partition_tokens);
@@ -134,9 +134,14 @@ size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int ma
  *   Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
  *   Computes out[s, h] = sum_t softmax_t(scale * q[s,h] . K[t]) V[t] over
  *   t < L_s with fp32 accumulation, rounded once to `dtype`.
- *   Sequences longer than `partition_tokens` (0 = 512; a multiple of 16 and
- *   of b) are split into partitions whose (max, normaliser, partial output)
- *   go to `workspace` and are merged by a second kernel.
+ *   Sequences longer than `partition_tokens` (a multiple of 16 and of b) are
+ *   split into partitions whose (max, normaliser, partial output) go to
+ *   `workspace` and are merged by a second kernel.  partition_tokens = 0
+ *   picks the size: 512 tokens (rounded down to a multiple of b), halved down
+ *   to 128 while B * ceil(Hq / 8) * ceil(max_blocks * b / size) stays below
+ *   608 (about four units per SM), so that short histories still spread over
+ *   the GPU.  It depends only on B, Hq, max_blocks and b, as the workspace
+ *   size does.
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
  *                 bytes, 16-byte aligned; may be NULL when that size is 0.
  *   Supported: D in {64, 128, 256}; Hq / Hkv in {1, 2, 4, 8}; b a multiple of

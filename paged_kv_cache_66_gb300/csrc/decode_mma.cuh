@@ -216,6 +216,19 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bs = p.block_size, P = p.partition_tokens;
     const int cap = p.max_blocks * bs;
+    const int tok0 = part * P;
+    const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks + tok0 / bs;
+    // The partition's table entries are requested together with the length (neither depends on
+    // the other), so the prologue costs one round trip before the first copy instead of two.
+    // Entries past the sequence's end are loaded (they lie inside the table row) but not used.
+    constexpr int PRE = (kMaxPartitionTokens / 16 + NW * 32 - 1) / (NW * 32);
+    const int ent_cap = min(P / bs, p.max_blocks - tok0 / bs);
+    int pre[PRE];
+#pragma unroll
+    for (int k = 0; k < PRE; ++k) {
+        const int i = tid + k * NW * 32;
+        pre[k] = i < ent_cap ? __ldg(trow + i) : -1;
+    }
     int L = __ldg(p.seq_lens + s);
     if (L < 0 || L > cap) {
         if (part == 0 && kvh0 == 0 && tid == 0) flag_error(p.err, PA_DEVERR_SEQLEN);
@@ -229,14 +242,12 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
         }
         return;
     }
-    const int tok0 = part * P;
     if (tok0 >= L) return;
     const int tok1 = min(L, tok0 + P);
     const int n_tiles = (tok1 - tok0 + C::TILE - 1) / C::TILE;
 
     int* tbl = reinterpret_cast<int*>(smem + C::tbl_off(hpc));
-    const int nblk = (tok1 - tok0 + bs - 1) / bs;
-    const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks + tok0 / bs;
+    const int nblk = (tok1 - tok0 + bs - 1) / bs;  // <= ent_cap
     // fused append: the partition holding position L - 1 writes that position's K/V rows of its
     // heads before any of its copies is issued.  Its loads (slot, table entry, the new rows) are
     // issued here, beside the table staging, so that they cost one round trip
@@ -262,13 +273,17 @@ __global__ void __launch_bounds__(MmaCfg<PE, D, G>::NW * 32)
             }
         }
     }
-    for (int i = tid; i < nblk; i += blockDim.x) {
-        int e = __ldg(trow + i);
-        if (e < 0 || e >= p.num_blocks) {
-            flag_error(p.err, PA_DEVERR_TABLE);
-            e = -1;
+#pragma unroll
+    for (int k = 0; k < PRE; ++k) {
+        const int i = tid + k * NW * 32;
+        if (i < nblk) {
+            int e = pre[k];
+            if (e < 0 || e >= p.num_blocks) {
+                flag_error(p.err, PA_DEVERR_TABLE);
+                e = -1;
+            }
+            tbl[i] = e;
         }
-        tbl[i] = e;
     }
     if constexpr (!F8) {
         // the pool stores are fenced against the async proxy, and the barrier below orders them
@@ -601,7 +616,7 @@ cudaError_t launch_mma(const DecodeParams& p_in, const CUtensorMap& kmap, const 
     if (configured_for != dev) {
         cudaError_t e = cudaFuncSetAttribute(decode_partition_mma<T, PE, D, G>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(C::smem_bytes(8192 / 16, 2)));
+                                             static_cast<int>(C::smem_bytes(kMaxPartitionTokens / 16, 2)));
         if (e != cudaSuccess) return e;
         configured_for = dev;
         cached_entries = -1;

@@ -17,7 +17,12 @@ __device__ int g_pa_error_word;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultPartition = 512;
-constexpr int kMaxPartition = 8192;
+constexpr int kMaxPartition = pa::kMaxPartitionTokens;
+constexpr int kMinAutoPartition = 128;
+// partition_tokens = 0: 512 tokens, halved (down to 128) while the launch would have fewer than
+// this many (sequence, KV head, partition) units -- about four per SM of a GB300 (152 SMs).
+// Short histories then still fill the GPU, and each CTA's serial chain of tiles is shorter.
+constexpr int64_t kAutoMinUnits = 4 * 152;
 
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
@@ -70,6 +75,20 @@ struct WsLayout {
     size_t acc_off;
     size_t total;
 };
+
+// The automatic partition size.  It depends only on arguments that pa_decode_workspace_size
+// also receives, so the two always agree.  The number of KV heads is not among them: the unit
+// count takes hq / 8 (the fewest KV heads a supported group allows) as a lower estimate.
+int auto_partition(int batch, int hq, int max_blocks, int b) {
+    int part = kDefaultPartition;
+    if (b > 0 && part % b != 0) part = b * (part / b > 0 ? part / b : 1);
+    const int64_t ctx = static_cast<int64_t>(max_blocks) * b;
+    const int64_t rows = static_cast<int64_t>(batch) * ((hq + 7) / 8);
+    while (part / 2 >= kMinAutoPartition && (part / 2) % b == 0 && (part / 2) % 16 == 0 &&
+           rows * ((ctx + part - 1) / part) < kAutoMinUnits)
+        part /= 2;
+    return part;
+}
 
 WsLayout ws_layout(int batch, int hq, int d, int max_blocks, int b, int part) {
     WsLayout w{};
@@ -172,7 +191,8 @@ pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int num_lay
 size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int max_blocks, int block_size,
                                 int partition_tokens) {
     if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks <= 0 || block_size <= 0) return 0;
-    const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    const int part =
+        partition_tokens == 0 ? auto_partition(batch, num_q_heads, max_blocks, block_size) : partition_tokens;
     if (part <= 0) return 0;
     return ws_layout(batch, num_q_heads, head_dim, max_blocks, block_size, part).total;
 }
@@ -195,7 +215,8 @@ pa_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
     if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
-    const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    const int part =
+        partition_tokens == 0 ? auto_partition(batch, num_q_heads, max_blocks, block_size) : partition_tokens;
     if (part <= 0 || part > kMaxPartition || part % 16 != 0 || part % block_size != 0) return PA_ERR_INVALID;
     if (static_cast<int64_t>(max_blocks) * block_size > (1LL << 30)) return PA_ERR_INVALID;
     if (batch == 0) return PA_OK;
@@ -317,7 +338,8 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (block_size % 16 != 0 || block_size > 256) return PA_ERR_UNSUPPORTED;
     if (static_cast<uint64_t>(num_blocks) * num_kv_heads * block_size >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
-    const int part = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    const int part =
+        partition_tokens == 0 ? auto_partition(batch, num_q_heads, max_blocks, block_size) : partition_tokens;
     if (part <= 0 || part > kMaxPartition || part % 16 != 0 || part % block_size != 0) return PA_ERR_INVALID;
     if (static_cast<int64_t>(max_blocks) * block_size > (1LL << 30)) return PA_ERR_INVALID;
     if (batch == 0) return PA_OK;

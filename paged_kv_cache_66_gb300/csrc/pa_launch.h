@@ -12,6 +12,7 @@
 namespace pa {
 
 constexpr int kMaxLayersPerLaunch = 64;
+constexpr int kMaxPartitionTokens = 8192;  // largest decode partition (a multiple of 16 and of b)
 
 struct PoolPtrs {
     void* k[kMaxLayersPerLaunch];

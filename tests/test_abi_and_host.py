@@ -93,6 +93,29 @@ def test_workspace_size():
     assert lib.pa_decode_workspace_size(8, 32, 128, 2048, 16, 0) == ml + rows * 128 * 4
 
 
+def test_auto_partition_size():
+    """partition_tokens = 0: 512 tokens, halved down to 128 while batch * ceil(Hq / 8) *
+    partitions stays under 608.  Checked through the workspace size, which uses the same rule."""
+    lib = _lib.load()
+
+    def same(shape, part):
+        return lib.pa_decode_workspace_size(*shape, 0) == lib.pa_decode_workspace_size(*shape, part)
+
+    def units(B, Hq, mb, b, part):
+        return B * -(-Hq // 8) * -(-mb * b // part)
+
+    # the long-context batch keeps 512 (8 x 4 x 64 units)
+    assert same((8, 32, 128, 2048, 16), 512) and units(8, 32, 2048, 16, 512) >= 608
+    # the Llama-3-8B-shaped batch of 32 histories under ~530 tokens: 512 -> 256 -> 128
+    assert units(32, 32, 34, 16, 512) < 608 and units(32, 32, 34, 16, 256) < 608
+    assert same((32, 32, 128, 34, 16), 128) and not same((32, 32, 128, 34, 16), 512)
+    # large batches keep 512; b = 256 stops at 256 (a partition is a multiple of b)
+    assert same((128, 32, 64, 270, 16), 512)
+    assert same((1, 8, 128, 4, 256), 256)
+    # b = 48: 480 tokens (the largest multiple of 48 up to 512), then 240
+    assert same((64, 32, 128, 40, 48), 480) and same((1, 8, 128, 40, 48), 240)
+
+
 def test_kernel_choices_accept_the_declared_values_only():
     """pa_set_decode_kernel / pa_set_prefill_kernel store a process-wide choice
     (host only): the enum values of include/pagedkv.h are taken, others refused."""
@@ -346,7 +369,9 @@ def test_decode_tile_to_table_entry_is_exact_over_the_accepted_shapes():
     tokens, block size) bound i and t; the quotient must be exact over all of them."""
     api_src = open(os.path.join(ROOT, "paged_kv_cache_66_gb300", "csrc", "pa_api.cu")).read()
     kern_src = open(os.path.join(ROOT, "paged_kv_cache_66_gb300", "csrc", "decode_mma.cuh")).read()
-    max_part = int(re.search(r"constexpr int kMaxPartition = (\d+);", api_src).group(1))
+    launch_src = open(os.path.join(ROOT, "paged_kv_cache_66_gb300", "csrc", "pa_launch.h")).read()
+    assert "constexpr int kMaxPartition = pa::kMaxPartitionTokens;" in api_src
+    max_part = int(re.search(r"constexpr int kMaxPartitionTokens = (\d+);", launch_src).group(1))
     max_b = int(re.search(r"block_size % 16 != 0 \|\| block_size > (\d+)\) return PA_ERR_UNSUPPORTED", api_src).group(1))
     assert "(65536u + tpb - 1) / tpb" in kern_src and "* inv_tpb) >> 16" in kern_src
     i = np.arange(max_part // 16, dtype=np.uint64)

@@ -57,7 +57,7 @@ class Workload:
     free_order: np.ndarray            # int32 permutation of range(num_blocks)
     setup_ops: list = field(default_factory=list)
     step_ops: list = field(default_factory=list)   # list (per decode step) of op lists
-    partition_tokens: int = 512
+    partition_tokens: int = 0         # decode partition tokens (0: the library's automatic size)
     prefix_owner: int = -1            # uid owning shared prefix content (-1: none)
     prefix_len: int = 0
     tolerance: float = 0.0            # max-abs tolerance of attention vs fp64
@@ -164,7 +164,7 @@ def config3(steps: int = 1, layers: int = 32, batch: int = 8, hist: int = 32767)
     seed = 1003
     wl = Workload(3, "longctx-f16-b8x32k", Hq=32, Hkv=8, D=128, b=16, dtype="f16",
                   num_blocks=20000, layers=layers, seed=seed,
-                  free_order=_perm(seed, 20000), tolerance=2e-3)
+                  free_order=_perm(seed, 20000), tolerance=2e-3, partition_tokens=512)
     for uid in range(batch):
         wl.setup_ops += [("create", uid), ("write", uid, hist)]
     wl.step_ops = [[("step", tuple(range(batch)))] for _ in range(steps)]
