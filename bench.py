@@ -687,7 +687,6 @@ def run_op(args, local):
                               "frac": alg / (ms / 1e3) / 1e9 / peak, "alg_bytes_per_launch": alg,
                               "peak_kind": f"{peak_kind} hbm_gbs"})
     elif args.op == "prefill":
-        api.pa_set_prefill_kernel(args.prefill_kernel)
         wl = wcfg.prefill_config(dtype=args.prefill_dtype, head_dim=args.prefill_head_dim)
         kp, vp, q = wcfg.prefill_inputs(wl, device=dev)
         tables = torch.as_tensor(wl.tables(), device=dev)
@@ -717,7 +716,8 @@ def run_op(args, local):
                     tokens_per_s=wl.batch * wl.chunk / (ms / 1e3),
                     roofline={"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
                               "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None,
-                              "kernel": f"pa_prefill ({args.prefill_kernel})"},
+                              "kernel": "pa_prefill (tcgen05, 128-key tiles)" if wl.D <= 128
+                              else "pa_prefill (tcgen05, Q in tensor memory)"},
                     gpu_launches=K)
     else:
         res = {}
@@ -774,7 +774,6 @@ def main():
     ap.add_argument("--partition", type=int, default=0, help="decode partition tokens (0: the workload's)")
     ap.add_argument("--copy-layers", type=int, default=32, help="--op copy: layers (pools of 4096 blocks each)")
     ap.add_argument("--copy-pairs", type=int, default=64, help="--op copy: copy-on-write pairs")
-    ap.add_argument("--prefill-kernel", default="auto", choices=["auto", "mma", "tc05", "tc05w"], help="--op prefill kernel")
     ap.add_argument("--prefill-head-dim", type=int, default=128, choices=[64, 128, 256],
                     help="--op prefill head dim (Hq 32, Hkv 8 kept)")
     ap.add_argument("--prefill-dtype", default="bf16", choices=["f16", "bf16"], help="--op prefill storage dtype")

@@ -315,27 +315,6 @@ pa_status pa_set_decode_kernel(pa_decode_kernel kernel);
  */
 pa_status pa_set_decode_heads_per_cta(int heads);
 
-/*
- * pa_set_prefill_kernel -- process-wide choice of the pa_prefill kernel (both
- * compute the same result within the attention tolerance):
- *   PA_PREFILL_AUTO  (default) PA_PREFILL_TC05W for D in {64, 128},
- *                    PA_PREFILL_TC05 for D = 256;
- *   PA_PREFILL_MMA   warp-level tensor-core kernel (mma m16n8k16), every D;
- *   PA_PREFILL_TC05  tcgen05 kernels (accumulators in tensor memory), 64-key
- *                    K/V tiles, every D (at D = 256 one query tile per CTA
- *                    with Q in tensor memory);
- *   PA_PREFILL_TC05W tcgen05 kernel with 128-key K/V tiles, D in {64, 128}.
- * With a forced kernel, pa_prefill returns PA_ERR_UNSUPPORTED for a D the
- * kernel does not cover.  Returns PA_ERR_INVALID for any other value.
- */
-typedef enum pa_prefill_kernel {
-    PA_PREFILL_AUTO = 0,
-    PA_PREFILL_MMA = 1,
-    PA_PREFILL_TC05 = 2,
-    PA_PREFILL_TC05W = 3
-} pa_prefill_kernel;
-
-pa_status pa_set_prefill_kernel(pa_prefill_kernel kernel);
 
 /*
  * pa_selftest_wait_timeout -- exercise the failure path of the bounded

@@ -39,7 +39,6 @@ SIGNATURES = {
                           _f32, _i32, _vp]),
     "pa_set_decode_kernel": (_i32, [_i32]),
     "pa_set_decode_heads_per_cta": (_i32, [_i32]),
-    "pa_set_prefill_kernel": (_i32, [_i32]),
     "pa_selftest_wait_timeout": (_i32, [_i32, _vp]),
     "pa_get_device_error": (_i32, [C.POINTER(C.c_int), _vp]),
     "pa_status_string": (C.c_char_p, [_i32]),

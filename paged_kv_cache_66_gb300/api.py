@@ -18,7 +18,7 @@ _TORCH_TO_ID = {torch.float32: DTYPE_IDS["f32"], torch.float16: DTYPE_IDS["f16"]
                 torch.bfloat16: DTYPE_IDS["bf16"]}
 
 __all__ = ["pa_kv_append", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc",
-           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_set_prefill_kernel", "pa_decode_append", "pa_get_device_error", "pa_status_string", "PagedKVError"]
+           "pa_kv_append_fp8", "pa_decode_fp8", "pa_set_decode_kernel", "pa_decode_append", "pa_get_device_error", "pa_status_string", "PagedKVError"]
 
 
 def _stream(stream):
@@ -231,18 +231,9 @@ def pa_set_decode_kernel(kernel: str) -> None:
     check(load().pa_set_decode_kernel(DECODE_KERNELS[kernel]), "pa_set_decode_kernel")
 
 
-PREFILL_KERNELS = {"auto": 0, "mma": 1, "tc05": 2, "tc05w": 3}
-
-
 def pa_set_decode_heads_per_cta(heads: int) -> None:
     """KV heads per CTA of the tensor-core decode kernel: 0 (choose per launch), 1 or 2."""
     check(load().pa_set_decode_heads_per_cta(int(heads)), "pa_set_decode_heads_per_cta")
-
-
-def pa_set_prefill_kernel(kernel: str) -> None:
-    """Process-wide pa_prefill kernel: "auto" (tcgen05 where it applies), "mma", "tc05" (64-key
-    tiles) or "tc05w" (128-key tiles, D = 128)."""
-    check(load().pa_set_prefill_kernel(PREFILL_KERNELS[kernel]), "pa_set_prefill_kernel")
 
 
 def pa_get_device_error(stream=None) -> int:

@@ -42,7 +42,6 @@ int* error_word() {
 
 std::atomic<int> g_decode_kernel{PA_DECODE_AUTO};
 std::atomic<int> g_decode_heads{0};
-std::atomic<int> g_prefill_kernel{PA_PREFILL_AUTO};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -139,13 +138,6 @@ pa_status pa_set_decode_heads_per_cta(int heads) {
     return PA_OK;
 }
 
-pa_status pa_set_prefill_kernel(pa_prefill_kernel kernel) {
-    if (kernel != PA_PREFILL_AUTO && kernel != PA_PREFILL_MMA && kernel != PA_PREFILL_TC05 &&
-        kernel != PA_PREFILL_TC05W)
-        return PA_ERR_INVALID;
-    g_prefill_kernel.store(kernel);
-    return PA_OK;
-}
 
 pa_status pa_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slot_mapping,
                        int64_t num_tokens, int64_t num_blocks, int num_kv_heads, int head_dim, int block_size,
@@ -420,7 +412,6 @@ pa_status pa_prefill(void* out, const void* q, const void* k_pool, const void* v
     p.hkv = num_kv_heads;
     p.block_size = block_size;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.kernel = g_prefill_kernel.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return from_cuda(dtype == PA_F16 ? pa::launch_prefill_f16(p, k_pool, v_pool, head_dim, max_query_len, st)
                                      : pa::launch_prefill_bf16(p, k_pool, v_pool, head_dim, max_query_len, st));

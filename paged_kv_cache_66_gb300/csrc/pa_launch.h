@@ -63,7 +63,6 @@ struct PrefillParams {
     int total_q;
     int hq, hkv, block_size;
     float scale_log2;             // scale * log2(e)
-    int kernel;                   // pa_prefill_kernel choice
 };
 
 // Launch `kernel` on `stream` allowing programmatic dependent launch (the

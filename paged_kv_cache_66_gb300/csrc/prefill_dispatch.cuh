@@ -1,12 +1,8 @@
-// Choice between the prefill kernels for one pa_prefill call: the tcgen05
-// kernels (128-key tiles, prefill_tc05w.cuh, at D in {64, 128}; 64-key tiles,
-// prefill_tc05.cuh, when forced; one query tile with Q in tensor memory,
-// prefill_tc05d.cuh, at D = 256) unless the caller forced the warp-level one
-// (prefill_mma.cuh), which covers every D.
+// The prefill kernel of one pa_prefill call: one per head dim -- 128-key K/V tiles with two
+// query tiles per CTA (prefill_tc05w.cuh) at D in {64, 128}, one query tile with Q in tensor
+// memory (prefill_tc05d.cuh) at D = 256.
 #pragma once
 
-#include "prefill_mma.cuh"
-#include "prefill_tc05.cuh"
 #include "prefill_tc05d.cuh"
 #include "prefill_tc05w.cuh"
 
@@ -16,16 +12,10 @@ template <typename T, int D, int G>
 cudaError_t launch_prefill_path(const PrefillParams& p, const CUtensorMap& km, const CUtensorMap& vm, int max_q,
                                 cudaStream_t stream) {
     if constexpr (D <= 128) {
-        if (p.kernel == PA_PREFILL_TC05W || p.kernel == PA_PREFILL_AUTO)
-            return launch_prefill_tc05w<T, D, G>(p, km, vm, max_q, stream);
-    }
-    if constexpr (D <= 128) {
-        if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05<T, D, G>(p, km, vm, max_q, stream);
+        return launch_prefill_tc05w<T, D, G>(p, km, vm, max_q, stream);
     } else {
-        if (p.kernel == PA_PREFILL_TC05W) return cudaErrorNotSupported;
-        if (p.kernel != PA_PREFILL_MMA) return launch_prefill_tc05d<T, G>(p, km, vm, max_q, stream);
+        return launch_prefill_tc05d<T, G>(p, km, vm, max_q, stream);
     }
-    return launch_prefill<T, D, G>(p, km, vm, max_q, stream);
 }
 
 template <typename T, int D>

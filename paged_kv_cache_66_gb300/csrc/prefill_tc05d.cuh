@@ -1,6 +1,6 @@
-// Paged prefill on tcgen05 for D = 256: the same operation, row packing and
-// softmax arithmetic as prefill_tc05.cuh ("25. Paged attention and prefix
-// caching", stretch exercise 4; "Chapter 7 Paged KV Cache and Memory
+// Paged prefill on tcgen05 for D = 256: the operation, row packing, masking and
+// base-2 lazy-rescale softmax of prefill_tc05w.cuh ("25. Paged attention and
+// prefix caching", stretch exercise 4; "Chapter 7 Paged KV Cache and Memory
 // Management", 4.1 step 3), laid out for the wide head.
 //
 // One CTA owns 128 query rows of one KV head.  Tensor memory holds O (256
@@ -9,7 +9,8 @@
 // and two 64-column S buffers; shared memory then holds only the K/V ring, three
 // stages of 64 keys (64 KiB each).  Per 64-key tile j:
 //   S_j = Q . K_j^T   tcgen05.mma M=128 N=64, A = Q (tensor memory), B = K_j (smem, K-major)
-//   softmax           one thread per row, as in prefill_tc05.cuh; P_j over the first half of S_j
+//   softmax           one thread per row: tcgen05.ld of its 64 scores, causal mask, running
+//                     max, P_j = 2^(s - m) rounded to the dtype over the first half of S_j
 //   O += P_j . V_j    tcgen05.mma M=128 N=256, A = P_j (tensor memory), B = V_j (smem, MN-major)
 // The MMA issuer runs one tile ahead: S(j+1) as soon as K_(j+1) has landed (its
 // S buffer held P(j-1), whose P . V was issued before; one thread's MMAs run in
@@ -20,7 +21,7 @@
 // tcgen05 load / store sits behind warp-uniform decisions.
 #pragma once
 
-#include "prefill_tc05.cuh"
+#include "prefill_tc05_common.cuh"
 
 namespace pa {
 

@@ -1,7 +1,16 @@
-// Paged prefill on tcgen05 with 128-key K/V tiles (D in {64, 128}): the same operation,
-// row packing and softmax arithmetic as prefill_tc05.cuh ("25. Paged attention
-// and prefix caching", stretch exercise 4; "Chapter 7 Paged KV Cache and Memory
-// Management", 4.1 step 3), laid out so that the score MMAs run at N = 128.
+// Paged prefill on the fifth-generation tensor cores (tcgen05.mma, accumulators in tensor
+// memory, operands staged in shared memory by TMA) for fp16 / bf16 pools with D in {64, 128}.
+//
+// A chunk of C new query tokens of one sequence -- its last C positions, whose K/V rows were
+// appended before the call -- attends causally to the sequence's paged history plus the chunk
+// ("25. Paged attention and prefix caching", stretch exercise 4; "Chapter 7 Paged KV Cache and
+// Memory Management", 4.1 step 3: the key at position p is visible to the query at position i
+// iff p <= i).  A row is a (chunk token, query head of the group) pair, the G heads of a token
+// side by side, so every K/V tile staged in shared memory serves all G heads of its KV head.
+// The softmax runs in base 2 with the scale folded in, and rescales O only when a row's max
+// grows by more than 2^8 (the reference cancels exactly in O / l).  Keys at or past a row's
+// position are masked; V rows past the sequence length (unwritten slots may hold anything) are
+// zeroed before they are used.  The score MMAs run at N = 128 keys.
 //
 // One CTA owns 256 query rows of one KV head as two 128-row tiles X = A, B that
 // share every 128-key K/V tile j.  Tensor memory holds O_A, O_B and one S buffer
@@ -27,7 +36,7 @@
 // every warp-collective tcgen05 load / store sits behind warp-uniform decisions.
 #pragma once
 
-#include "prefill_tc05.cuh"
+#include "prefill_tc05_common.cuh"
 
 namespace pa {
 namespace tc05 {

@@ -117,20 +117,16 @@ def test_auto_partition_size():
 
 
 def test_kernel_choices_accept_the_declared_values_only():
-    """pa_set_decode_kernel / pa_set_prefill_kernel store a process-wide choice
+    """pa_set_decode_kernel / pa_set_decode_heads_per_cta store a process-wide choice
     (host only): the enum values of include/pagedkv.h are taken, others refused."""
     lib = _lib.load()
-    for k in (0, 1, 2, 3):
-        assert lib.pa_set_prefill_kernel(k) == 0
-    assert lib.pa_set_prefill_kernel(4) == 1                # PA_ERR_INVALID
-    assert lib.pa_set_prefill_kernel(-1) == 1
     for k in (0, 1, 2):
         assert lib.pa_set_decode_kernel(k) == 0
     assert lib.pa_set_decode_kernel(3) == 1
     for h in (0, 1, 2):
         assert lib.pa_set_decode_heads_per_cta(h) == 0
     assert lib.pa_set_decode_heads_per_cta(3) == 1 and lib.pa_set_decode_heads_per_cta(-1) == 1
-    assert lib.pa_set_prefill_kernel(0) == 0 and lib.pa_set_decode_kernel(0) == 0
+    assert lib.pa_set_decode_kernel(0) == 0
     assert lib.pa_set_decode_heads_per_cta(0) == 0
 
 

@@ -101,23 +101,10 @@ CASES = [
 ]
 
 
-@pytest.fixture(params=["mma", "tc05", "tc05w"])
-def kernel(request, api):
-    api.pa_set_prefill_kernel(request.param)
-    yield request.param
-    api.pa_set_prefill_kernel("auto")
-
-
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("case", CASES)
-def test_prefill_matches_oracle(api, kernel, dtype, case):
+def test_prefill_matches_oracle(api, dtype, case):
     Hq, Hkv, D, b, lengths, chunks = case
-    if kernel == "tc05w" and D == 256:
-        K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype, seed=1)
-        with pytest.raises(api.PagedKVError) as e:
-            _run(api, K, V, q, tables, lens, qstart, 0.1)
-        assert e.value.status == 2
-        return
     K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype,
                                            seed=hash((Hq, D, b, len(lengths))) & 0xFFFF)
     scale = 1 / math.sqrt(D)
@@ -129,7 +116,7 @@ def test_prefill_matches_oracle(api, kernel, dtype, case):
     _check(got.double().numpy(), want, V.double().numpy(), dtype, _visible(lengths, chunks))
 
 
-def test_prefill_chunk_of_one_equals_decode(api, kernel):
+def test_prefill_chunk_of_one_equals_decode(api):
     """A one-row chunk is decode at the sequence's last position."""
     Hq, Hkv, D, b = 32, 8, 128, 16
     lengths = [513, 40, 1]
@@ -143,8 +130,9 @@ def test_prefill_chunk_of_one_equals_decode(api, kernel):
     assert (got - out.cpu()).abs().max().item() <= 2e-3
 
 
-def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api, kernel):
-    Hq, Hkv, D, b = 8, 2, (128 if kernel == "tc05w" else 64), 16
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api, D):
+    Hq, Hkv, b = 8, 2, 16
     K, V, q, tables, lens, qstart = _setup([20, 30], [5, 6], Hq, Hkv, D, b, torch.float16, seed=11)
     lens[0] = 3                                           # chunk of 5 > length 3
     got = _run(api, K, V, q, tables, lens, qstart, 0.125)
@@ -155,8 +143,9 @@ def test_prefill_inconsistent_chunk_is_flagged_and_skipped(api, kernel):
     assert np.abs(got[5:].double().numpy() - want).max() <= 2e-3
 
 
-def test_prefill_bad_table_entry_is_flagged(api, kernel):
-    Hq, Hkv, D, b = 8, 2, (128 if kernel == "tc05w" else 64), 16
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_bad_table_entry_is_flagged(api, D):
+    Hq, Hkv, b = 8, 2, 16
     K, V, q, tables, lens, qstart = _setup([40], [40], Hq, Hkv, D, b, torch.float16, seed=12)
     tables[0, 1] = K.shape[0] + 7
     _run(api, K, V, q, tables, lens, qstart, 0.125)
@@ -189,14 +178,15 @@ def test_prefill_f32_unsupported(api):
     assert e.value.status == 2
 
 
+@pytest.mark.parametrize("head_dim", [128, 64, 256])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_prefill_bench_workload_sampled_rows(api, kernel, dtype):
+def test_prefill_bench_workload_sampled_rows(api, dtype, head_dim):
     """The benchmark's launch (8 chunks of 1024 over 3072 cached tokens, Llama-3-8B
     layer shape), inputs generated on the device as the benchmark does; sampled
     rows checked one by one against the oracle."""
     from oracle import attention as oatt
     from workload import configs as wcfg
-    wl = wcfg.prefill_config(dtype=dtype)
+    wl = wcfg.prefill_config(dtype=dtype, head_dim=head_dim)
     kp, vp, q = wcfg.prefill_inputs(wl, device="cuda")
     tables = torch.as_tensor(wl.tables(), device="cuda")
     lens = torch.full((wl.batch,), wl.length, dtype=torch.int32, device="cuda")
