@@ -146,3 +146,40 @@ def test_prefill_mistakes_are_caught(monkeypatch, bad):
         except AssertionError:
             caught += 1
     assert caught >= 1
+
+
+def test_tree_eviction_of_inner_nodes_is_caught(monkeypatch):
+    """A prefix tree that drops any idle node (not only leaves) strands the longer prefixes
+    below it: the hand-worked divergence case and the trace invariants catch it."""
+    from oracle import prefix_tree as pt
+    from tests import test_oracle_prefix_tree as tree_pins
+
+    def evict_any(self, blocks_wanted):
+        alloc = self.tables.allocator
+        while alloc.num_free < int(blocks_wanted):
+            idle = [n for n in self.nodes() if alloc.refs[n.block] == 1]
+            if not idle:
+                return
+            victim = min(idle, key=lambda n: n.used)
+            del victim.parent.children[victim.label]
+            alloc.release(victim.block)
+
+    monkeypatch.setattr(pt.BlockPrefixTree, "evict", evict_any)
+    with pytest.raises(AssertionError):
+        tree_pins.test_eviction_takes_leaves_where_the_flat_table_strands_a_prefix()
+    with pytest.raises(AssertionError):
+        tree_pins.test_tree_invariants_hold_on_traces_with_eviction(0)
+
+
+def test_tree_attach_without_prefill_margin_is_caught(monkeypatch):
+    """Reusing every full block of the prompt (no token left to prefill) is caught."""
+    from oracle import prefix_tree as pt
+    from tests import test_oracle_prefix_tree as tree_pins
+    orig = pt.BlockPrefixTree.attach
+
+    def attach_all(self, seq, prompt):
+        return orig(self, seq, list(prompt) + [None])    # one phantom token: the last block counts
+
+    monkeypatch.setattr(pt.BlockPrefixTree, "attach", attach_all)
+    with pytest.raises(AssertionError):
+        tree_pins.test_at_least_one_prompt_token_is_left_to_prefill()
