@@ -135,6 +135,32 @@ int64_t pa_host_hprefix_entries(const pa_host* h);
  * and returns the number of entries (-1 on invalid arguments). */
 int64_t pa_host_hprefix_blocks(const pa_host* h, int32_t* blocks_out, int64_t capacity);
 
+/* Block prefix tree: the radix-tree form of the prefix table ("Prefix caching",
+ * closing paragraph: a radix tree over all cached prefixes; "Модуль 09",
+ * RadixAttention: the shared prefixes of all past requests form a tree kept
+ * by least-recently-used eviction).  One node per cached full block, reached
+ * from its parent by an edge labelled with the block's token ids.
+ * attach / remember follow the rules of the tuple-keyed table above (with no
+ * eviction the two make the same decisions): attach walks the prompt's full
+ * blocks from the root, leaving at least one token to prefill, shares each
+ * matched block and marks the matched nodes most recently used in walk
+ * order; remember descends through cached blocks (recency unchanged) and
+ * hangs the sequence's remaining full blocks below them, taking the tree's
+ * own reference.  evict drops only leaves -- nodes no cached block extends --
+ * least recently used first and only while the tree alone holds the block,
+ * until `blocks_wanted` blocks are free; a parent whose last child went
+ * becomes a leaf in turn.  The tree is independent of the other two tables.
+ * NULL handles or negative sizes give PA_ERR_INVALID; remember gives
+ * PA_ERR_INVALID when `seq` holds fewer than n / block_size blocks. */
+pa_status pa_host_tprefix_attach(pa_host* h, int64_t seq, const int64_t* prompt, int64_t n, int64_t* reused);
+pa_status pa_host_tprefix_remember(pa_host* h, int64_t seq, const int64_t* tokens, int64_t n);
+pa_status pa_host_tprefix_evict(pa_host* h, int64_t blocks_wanted);
+/* Number of cached nodes (-1 for a NULL handle). */
+int64_t pa_host_tprefix_nodes(const pa_host* h);
+/* Cached block ids in ascending order; writes at most `capacity` and returns
+ * the number of cached blocks (-1 on invalid arguments). */
+int64_t pa_host_tprefix_blocks(const pa_host* h, int32_t* blocks_out, int64_t capacity);
+
 #ifdef __cplusplus
 }
 #endif

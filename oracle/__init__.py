@@ -16,6 +16,8 @@ Modules:
   blocks     -- BlockAllocator, SeqTables, KeyedPrefixIndex / PrefixTable
                 ([P1] allocator, paged cache, prefix caching; written from the
                 invariants the pages fix, readings in the module header)
+  prefix_hash -- SHA-256 chain keys and the prefix table keyed by them ([P1] prefix caching)
+  prefix_tree -- the block prefix tree, the radix-tree form of the prefix cache
   cache_ops  -- K/V scatter through slots and block copy-on-write ([P1] update/reserve)
   attention  -- decode attention by its definition (fp64), the blockwise
                 online-softmax / split merge used only as a cross-check ([P5] 4.2)

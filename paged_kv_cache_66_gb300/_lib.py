@@ -69,6 +69,11 @@ SIGNATURES = {
     "pa_host_hprefix_evict": (_i32, [_vp, _i64]),
     "pa_host_hprefix_entries": (_i64, [_vp]),
     "pa_host_hprefix_blocks": (_i64, [_vp, _p32, _i64]),
+    "pa_host_tprefix_attach": (_i32, [_vp, _i64, _p64, _i64, _p64]),
+    "pa_host_tprefix_remember": (_i32, [_vp, _i64, _p64, _i64]),
+    "pa_host_tprefix_evict": (_i32, [_vp, _i64]),
+    "pa_host_tprefix_nodes": (_i64, [_vp]),
+    "pa_host_tprefix_blocks": (_i64, [_vp, _p32, _i64]),
 }
 
 _LIB = None

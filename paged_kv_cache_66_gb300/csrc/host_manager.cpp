@@ -13,7 +13,9 @@
 #include <deque>
 #include <list>
 #include <new>
+#include <set>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "../../include/pagedkv_host.h"
@@ -82,6 +84,16 @@ ChainKey chain_next(const ChainKey& parent, const int64_t* tokens, int block_siz
     return k;
 }
 
+// A node of the block prefix tree: one cached full block, reached from its parent by an
+// edge labelled with the block's token ids.  Node 0 is the root (the empty prefix).
+struct TreeNode {
+    int32_t parent = -1;
+    int32_t block = -1;
+    int64_t used = 0;               // recency stamp: larger = more recently used
+    std::vector<int64_t> label;     // the block's block_size token ids
+    std::unordered_map<std::vector<int64_t>, int32_t, VecHash> children;
+};
+
 }  // namespace
 
 struct pa_host {
@@ -98,6 +110,13 @@ struct pa_host {
     // hash-chain prefix table: chain key -> (block, position in its own LRU list)
     std::list<ChainKey> hlru;
     std::unordered_map<ChainKey, std::pair<int32_t, std::list<ChainKey>::iterator>, ChainKeyHash> hentries;
+    // block prefix tree: nodes (slot 0 the root, freed slots reused), every non-root leaf ordered
+    // by (recency stamp, node), and the stamp clock
+    std::vector<TreeNode> tnodes = std::vector<TreeNode>(1);
+    std::vector<int32_t> tfree;
+    std::set<std::pair<int64_t, int32_t>> tleaves;
+    int64_t tclock = 0;
+    int64_t tcount = 0;
 
     int64_t blocks_needed(int64_t tokens) const { return (tokens + block_size - 1) / block_size; }
 
@@ -494,6 +513,131 @@ int64_t pa_host_hprefix_blocks(const pa_host* h, int32_t* blocks_out, int64_t ca
         ++i;
     }
     return i;
+}
+
+// ------------------------------------------------------------------ block prefix tree
+// The radix-tree form of the prefix table: rules in include/pagedkv_host.h.
+
+namespace {
+
+bool tree_is_leaf(const pa_host* h, int32_t node) { return node != 0 && h->tnodes[node].children.empty(); }
+
+// stamp `node` most recently used, keeping the leaf order in step
+void tree_touch(pa_host* h, int32_t node) {
+    TreeNode& t = h->tnodes[node];
+    const bool leaf = tree_is_leaf(h, node);
+    if (leaf) h->tleaves.erase({t.used, node});
+    t.used = ++h->tclock;
+    if (leaf) h->tleaves.insert({t.used, node});
+}
+
+}  // namespace
+
+pa_status pa_host_tprefix_attach(pa_host* h, int64_t seq, const int64_t* prompt, int64_t n, int64_t* reused) {
+    if (!h || n < 0 || (n > 0 && !prompt)) return PA_ERR_INVALID;
+    if (h->seqs.count(seq)) return PA_ERR_EXISTS;
+    const int64_t size = h->block_size;
+    std::vector<int32_t> path;
+    int32_t node = 0;
+    std::vector<int64_t> label;
+    for (int64_t r = 0; r + size <= n - 1; r += size) {  // at least one prompt token is left to prefill
+        label.assign(prompt + r, prompt + r + size);
+        auto it = h->tnodes[node].children.find(label);
+        if (it == h->tnodes[node].children.end()) break;
+        node = it->second;
+        path.push_back(node);
+    }
+    Seq s;
+    for (int32_t v : path) {
+        tree_touch(h, v);
+        h->refs[h->tnodes[v].block] += 1;  // cached blocks are live
+        s.table.push_back(h->tnodes[v].block);
+    }
+    s.length = static_cast<int64_t>(path.size()) * size;
+    if (reused) *reused = s.length;
+    h->seqs.emplace(seq, std::move(s));
+    return PA_OK;
+}
+
+pa_status pa_host_tprefix_remember(pa_host* h, int64_t seq, const int64_t* tokens, int64_t n) {
+    if (!h || n < 0 || (n > 0 && !tokens)) return PA_ERR_INVALID;
+    const Seq* s = h->find(seq);
+    if (!s) return PA_ERR_NOT_FOUND;
+    const int64_t size = h->block_size;
+    const int64_t full = n / size;
+    if (full > static_cast<int64_t>(s->table.size())) return PA_ERR_INVALID;
+    int32_t node = 0;
+    std::vector<int64_t> label;
+    for (int64_t i = 0; i < full; ++i) {
+        label.assign(tokens + i * size, tokens + (i + 1) * size);
+        auto it = h->tnodes[node].children.find(label);
+        if (it != h->tnodes[node].children.end()) {  // cached: descend, recency unchanged
+            node = it->second;
+            continue;
+        }
+        int32_t v;
+        if (!h->tfree.empty()) {
+            v = h->tfree.back();
+            h->tfree.pop_back();
+        } else {
+            v = static_cast<int32_t>(h->tnodes.size());
+            h->tnodes.emplace_back();
+        }
+        if (tree_is_leaf(h, node)) h->tleaves.erase({h->tnodes[node].used, node});  // gains a child
+        TreeNode& t = h->tnodes[v];
+        t.parent = node;
+        t.block = s->table[static_cast<size_t>(i)];
+        t.used = ++h->tclock;
+        t.label = label;
+        t.children.clear();
+        h->tnodes[node].children.emplace(label, v);
+        h->tleaves.insert({t.used, v});
+        h->refs[t.block] += 1;  // the tree's own reference
+        ++h->tcount;
+        node = v;
+    }
+    return PA_OK;
+}
+
+pa_status pa_host_tprefix_evict(pa_host* h, int64_t blocks_wanted) {
+    if (!h) return PA_ERR_INVALID;
+    // Leaves ahead of the cursor are held by a sequence; evicting other leaves does not change
+    // that, so the scan never has to look back -- except at a parent that just became a leaf
+    // with an older stamp, where it resumes.
+    auto it = h->tleaves.begin();
+    while (static_cast<int64_t>(h->free_list.size()) < blocks_wanted && it != h->tleaves.end()) {
+        const int32_t v = it->second;
+        TreeNode& t = h->tnodes[v];
+        if (h->refs[t.block] != 1) {
+            ++it;
+            continue;
+        }
+        const int32_t parent = t.parent;
+        h->tnodes[parent].children.erase(t.label);
+        it = h->tleaves.erase(it);
+        h->release(t.block);
+        t.label.clear();
+        t.block = -1;
+        h->tfree.push_back(v);
+        --h->tcount;
+        if (tree_is_leaf(h, parent)) {
+            auto ins = h->tleaves.insert({h->tnodes[parent].used, parent}).first;
+            if (it == h->tleaves.end() || *ins < *it) it = ins;
+        }
+    }
+    return PA_OK;
+}
+
+int64_t pa_host_tprefix_nodes(const pa_host* h) { return h ? h->tcount : -1; }
+
+int64_t pa_host_tprefix_blocks(const pa_host* h, int32_t* blocks_out, int64_t capacity) {
+    if (!h || capacity < 0 || (capacity > 0 && !blocks_out)) return -1;
+    std::vector<int32_t> blocks;
+    for (size_t v = 1; v < h->tnodes.size(); ++v)
+        if (h->tnodes[v].block >= 0) blocks.push_back(h->tnodes[v].block);
+    std::sort(blocks.begin(), blocks.end());
+    for (int64_t i = 0; i < static_cast<int64_t>(blocks.size()) && i < capacity; ++i) blocks_out[i] = blocks[i];
+    return static_cast<int64_t>(blocks.size());
 }
 
 }  // extern "C"

@@ -211,3 +211,28 @@ class HostBlockManager:
         out = np.zeros(max(n, 1), dtype=np.int32)
         self._lib.pa_host_hprefix_blocks(self._h, _p32(out), n)
         return out[:n].tolist()
+
+    # ------------------------------------------------------ block prefix tree
+    def tprefix_attach(self, seq: int, prompt) -> int:
+        p = np.ascontiguousarray(np.asarray(prompt, dtype=np.int64))
+        out = np.zeros(1, dtype=np.int64)
+        _raise(self._lib.pa_host_tprefix_attach(self._h, int(seq), _p64(p), p.shape[0], _p64(out)), "attach")
+        return int(out[0])
+
+    def tprefix_remember(self, seq: int, tokens) -> None:
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+        _raise(self._lib.pa_host_tprefix_remember(self._h, int(seq), _p64(t), t.shape[0]), "remember")
+
+    def tprefix_evict(self, blocks_wanted: int) -> None:
+        _raise(self._lib.pa_host_tprefix_evict(self._h, int(blocks_wanted)), "evict")
+
+    @property
+    def tprefix_nodes(self) -> int:
+        return int(self._lib.pa_host_tprefix_nodes(self._h))
+
+    def tprefix_blocks(self) -> list:
+        """Cached block ids, ascending."""
+        n = int(self._lib.pa_host_tprefix_blocks(self._h, None, 0))
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._lib.pa_host_tprefix_blocks(self._h, _p32(out), n)
+        return out[:n].tolist()
