@@ -697,14 +697,24 @@ def run_op(args, local):
         for _ in range(args.warmup):
             api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
         torch.cuda.synchronize()
+        # at least K launches, and enough for ~0.5 s so the clock sampler sees the region (a
+        # dense kernel on this part may run under its power cap: the clocks say)
+        t0 = time.perf_counter()
+        flush.zero_()
+        api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
+        torch.cuda.synchronize()
+        K = max(K, int(np.ceil(0.5 / max(time.perf_counter() - t0, 1e-6))))
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        clocks = ClockSampler(local)
         for a, b_ in ev:
             flush.zero_()
             a.record(stream)
             api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
             b_.record(stream)
         torch.cuda.synchronize()
+        clk = clocks.stop()
         ms = sum(a.elapsed_time(b_) for a, b_ in ev) / K
+        line["steps"] = K
         flops = 4 * wl.D * wl.Hq * wl.causal_pairs()
         tf = flops / (ms / 1e3) / 1e12
         tpeak, tkind = _tensor_peak()
@@ -718,6 +728,7 @@ def run_op(args, local):
                               "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None,
                               "kernel": "pa_prefill (tcgen05, 128-key tiles)" if wl.D <= 128
                               else "pa_prefill (tcgen05, Q in tensor memory)"},
+                    clocks={k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
                     gpu_launches=K)
     else:
         res = {}
