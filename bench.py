@@ -533,7 +533,7 @@ def run_ours(args, ws, rank, local):
     }
     if configs is not None:
         line["configs"] = configs
-    if not args.no_cpu_baseline and ws >= 1 and rank == 0:
+    if not args.no_cpu_baseline and ws == 1 and rank == 0:   # the host baseline: one GPU only
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
 
