@@ -54,18 +54,13 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
     };
     int r = blockIdx.x * rpi + lr;
     for (; r + step < rows; r += 2 * step) {
+        // the rows' data is requested together with their slots (the rows lie inside k and v
+        // whatever the slots say); only the stores wait for the slots
+        const size_t s0 = static_cast<size_t>(r) * vpr + c, s1 = static_cast<size_t>(r + step) * vpr + c;
+        const uint4 k0 = __ldg(k + s0), v0 = __ldg(v + s0);
+        const uint4 k1 = __ldg(k + s1), v1 = __ldg(v + s1);
         size_t d0 = 0, d1 = 0;
         const bool ok0 = place(r, d0), ok1 = place(r + step, d1);
-        const size_t s0 = static_cast<size_t>(r) * vpr + c, s1 = static_cast<size_t>(r + step) * vpr + c;
-        uint4 k0, v0, k1, v1;
-        if (ok0) {
-            k0 = __ldg(k + s0);
-            v0 = __ldg(v + s0);
-        }
-        if (ok1) {
-            k1 = __ldg(k + s1);
-            v1 = __ldg(v + s1);
-        }
         if (ok0) {
             k_pool[d0] = k0;
             v_pool[d0] = v0;
@@ -141,6 +136,13 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const Tin* __restric
         const int rk = i / vpr;
         const int kind = rk & 1, r = rk >> 1;
         const int t = r / hkv, h = r - t * hkv;
+        // the row's 16 inputs and its scale are requested together with the slot (they lie inside
+        // k / v and the scale array whatever the slot says); only the store waits for the slot
+        const Tin* src = (kind == 0 ? k : v) + (static_cast<size_t>(r) * vpr + c) * 16;
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = Elt<Tin>::to_f32(src[j]);
+        const float sc = __ldg((kind == 0 ? k_scale : v_scale) + h);
         const int64_t slot = __ldg(slots + t);
         if (slot < 0) continue;
         if (slot >= num_slots) {
@@ -148,13 +150,11 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const Tin* __restric
             continue;
         }
         const int64_t blk = slot / block_size, off = slot - blk * block_size;
-        const Tin* src = (kind == 0 ? k : v) + (static_cast<size_t>(r) * vpr + c) * 16;
-        const float sc = __ldg((kind == 0 ? k_scale : v_scale) + h);
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float a = Elt<Tin>::to_f32(src[4 * j]) / sc, b = Elt<Tin>::to_f32(src[4 * j + 1]) / sc;
-            const float cc = Elt<Tin>::to_f32(src[4 * j + 2]) / sc, d = Elt<Tin>::to_f32(src[4 * j + 3]) / sc;
+            const float a = x[4 * j] / sc, b = x[4 * j + 1] / sc;
+            const float cc = x[4 * j + 2] / sc, d = x[4 * j + 3] / sc;
             const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
             const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(cc, d), __NV_SATFINITE, __NV_E4M3);
             w[j] = (lo & 0xFFFFu) | (hi << 16);
