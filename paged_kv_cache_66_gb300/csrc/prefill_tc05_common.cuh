@@ -62,6 +62,29 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                  : "memory");
 }
 
+// max of three (one instruction on sm_100+)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// (y0, y1) = (x0 * m + b, x1 * m + b), one packed fp32 FMA (each lane rounded once, as fmaf)
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float m, float b) {
+    asm("{\n\t.reg .b64 x, mm, bb, y;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 mm, {%4, %4};\n\t"
+        "mov.b64 bb, {%5, %5};\n\tfma.rn.f32x2 y, x, mm, bb;\n\tmov.b64 {%0, %1}, y;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(x0), "f"(x1), "f"(m), "f"(b));
+}
+
+// (s0, s1) += (a0, a1), one packed fp32 add
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 s, a;\n\tmov.b64 s, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\t"
+        "add.rn.f32x2 s, s, a;\n\tmov.b64 {%0, %1}, s;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -76,6 +99,12 @@ __device__ __forceinline__ void ld32(uint32_t addr, uint32_t* r) {
         : "r"(addr));
 }
 
+__device__ __forceinline__ void st8(uint32_t addr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(addr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void st32(uint32_t addr, const uint32_t* r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -84,15 +113,6 @@ __device__ __forceinline__ void st32(uint32_t addr, const uint32_t* r) {
         "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
         "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
         "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void st16(uint32_t addr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16};" ::"r"(addr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 

@@ -330,22 +330,25 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             m = mx;
         }
         const float ms = m == -INFINITY ? 0.f : m;
-        // P = 2^(v * mul - m) in one FFMA and one ex2 (interior: v raw, mul = scale; masked: v
-        // pre-scaled, mul = 1); key c at column c / 2 of S buffer sb, over this lane's own scores
+        // P = 2^(v * mul - m), pairs of keys in one packed FMA and add (interior: v raw, mul =
+        // scale; masked: v pre-scaled, mul = 1); key c at column c / 2 of S buffer sb, over this
+        // lane's own scores, in 8-word stores (each issued before the next words' exponentials)
         const float mul = interior ? sl2 : 1.f;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
-            uint32_t pw[16];
+        for (int hq = 0; hq < 4; ++hq) {
+            uint32_t pw[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = hq * 32 + 2 * i;
-                const float e0 = tc05::fast_exp2(fmaf(__uint_as_float(sr[c]), mul, -ms));
-                const float e1 = tc05::fast_exp2(fmaf(__uint_as_float(sr[c + 1]), mul, -ms));
-                ls[i & 3] += e0 + e1;
+            for (int i = 0; i < 8; ++i) {
+                const int c = hq * 16 + 2 * i;
+                float x0, x1;
+                tc05::fma2(x0, x1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), mul, -ms);
+                const float e0 = tc05::fast_exp2(x0);
+                const float e1 = tc05::fast_exp2(x1);
+                tc05::add2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], e0, e1);
                 pw[i] = pack2<T>(e0, e1);
             }
-            tc05::st16(sa + hq * 16, pw);
+            tc05::st8(sa + hq * 8, pw);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // V rows of keys past the sequence or of sub-tiles not loaded may hold anything: zero them
