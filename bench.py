@@ -305,6 +305,25 @@ def cpu_baseline(wl, budget_s: float = 15.0):
 
 # ------------------------------------------------------------------ our arm
 
+L2_FLUSH_DOC = ("L2 flushed before every timed step: a 256 MiB write, then a 256 MiB read of another buffer "
+                "so that the write's dirty lines are written back before the step, not inside it")
+
+
+class L2Flush:
+    """Evicts L2 (129 MB) before a timed region: a 256 MiB write, then a read of another 256 MiB.
+    The read pass leaves L2 holding clean lines of an unrelated buffer; without it, each miss of
+    the timed kernel would first write back one dirty line of the flush, which charges the
+    flush's own traffic to the kernel."""
+
+    def __init__(self, dev, read_mib: int = 256):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(read_mib << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=True, flush_l2=False,
                     min_seconds=0.0):
     """Time ``steps`` decode steps of ``wl`` on the device, inputs resident in HBM.
@@ -313,8 +332,8 @@ def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=
     ``flush_l2`` the timed steps run back to back (for histories far larger than
     L2) and only the decode launches of the last timed steps are bracketed by
     events (an event between two launches ends their programmatic overlap).
-    With ``flush_l2`` (histories that fit in L2) a 256 MiB write evicts L2
-    before every timed step, each step is bracketed by its own events, and the
+    With ``flush_l2`` (histories that fit in L2) L2 is evicted before every
+    timed step (``L2Flush``), each step is bracketed by its own events, and the
     step time is the sum of those.
 
     With ``min_seconds`` the ``steps`` planned steps are executed in turn as
@@ -332,7 +351,7 @@ def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=
     plans = [rp.plan_step(i) for i in range(total_steps)]
     dsteps = [rp.device_step(p) for p in plans]
     outs = [torch.empty((len(plans[0].uids), wl.Hq, wl.D), dtype=wl.torch_dtype, device=dev) for _ in rp.layers]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
+    flush = L2Flush(dev) if flush_l2 else None
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     # The Python collector is left running: pausing it around the timed regions (gc.disable, with
@@ -346,7 +365,7 @@ def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=
         t0 = time.perf_counter()
         for j in range(steps):
             if flush_l2:
-                flush.zero_()
+                flush()
             rp.run_step(dsteps[warmup + j], outs)
         torch.cuda.synchronize()
         reps = max(1, int(np.ceil(min_seconds / max(time.perf_counter() - t0, 1e-6))))
@@ -372,7 +391,7 @@ def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=
         B, width = ds.tables.shape
         wsbuf = rp.workspace_for(B, width)
         if flush_l2:
-            flush.zero_()
+            flush()
             ev_step[j][0].record(stream)
         torch.cuda.nvtx.range_push(f"decode step {j}")
         if ds.pairs.shape[0]:
@@ -443,8 +462,8 @@ def _secondary(spec, steps, warmup, dev, ws, peak):
         "effective_kv_gbs": m["kv_bytes"] / (m["dev_ms_max"] / 1e3) / 1e9,
         "seq_steps_per_s": m["B"] * steps / (m["dev_ms_max"] / 1e3),
         "kv_bytes_per_decode": {"effective": m["effective"], "unique": m["unique"]},
-        "l2": ("L2 flushed (256 MiB write) before every timed step; each step timed by its own events"
-               if small else "history larger than L2 (no flush needed)"),
+        "l2": (L2_FLUSH_DOC + "; each step timed by its own events" if small
+               else "history larger than L2 (no flush needed)"),
         "roofline": {"bound": "hbm", "peak": peak, "unit": "GB/s",
                      "alg_bytes_per_launch": m["alg"], "avg_launch_ms": m["dec_avg_ms"],
                      "median_launch_ms": m["dec_med_ms"],
@@ -508,8 +527,8 @@ def run_ours(args, ws, rank, local):
                    "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
                    "partition_tokens": wl.partition_tokens if not args.partition else args.partition,
                    "kv_cache": "e4m3" if args.kv == "fp8" else wl.dtype,
-                   "l2": ("L2 flushed (256 MiB write) before every timed step; each step timed by its own events"
-                          if args.flush_l2 else "inputs larger than L2 (no flush needed)"),
+                   "l2": (L2_FLUSH_DOC + "; each step timed by its own events" if args.flush_l2
+                          else "inputs larger than L2 (no flush needed)"),
                    "parallelism": f"replicas x{ws}"},
         "seq_steps_per_s": seq_steps,
         "kv_bytes_per_decode": {"effective": m["effective"], "unique": m["unique"],
@@ -693,21 +712,21 @@ def run_op(args, local):
         lens = torch.full((wl.batch,), wl.length, dtype=torch.int32, device=dev)
         qstart = torch.as_tensor(wl.qstart(), device=dev)
         out = torch.empty_like(q)
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2, rewritten before each launch
+        flush = L2Flush(dev)  # before each launch
         for _ in range(args.warmup):
             api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
         torch.cuda.synchronize()
         # at least K launches, and enough for ~0.5 s so the clock sampler sees the region (a
         # dense kernel on this part may run under its power cap: the clocks say)
         t0 = time.perf_counter()
-        flush.zero_()
+        flush()
         api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
         torch.cuda.synchronize()
         K = max(K, int(np.ceil(0.5 / max(time.perf_counter() - t0, 1e-6))))
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         clocks = ClockSampler(local)
         for a, b_ in ev:
-            flush.zero_()
+            flush()
             a.record(stream)
             api.pa_prefill(out, q, kp, vp, tables, lens, qstart, wl.scale, max_query_len=wl.chunk)
             b_.record(stream)
@@ -722,7 +741,7 @@ def run_op(args, local):
                     ms_per_launch=ms, dtype=wl.dtype,
                     config={"workload": wl.name, "batch": wl.batch, "history": wl.history, "chunk": wl.chunk,
                             "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
-                            "l2": "flushed before every launch (256 MiB write)"},
+                            "l2": L2_FLUSH_DOC.replace("step", "launch")},
                     tokens_per_s=wl.batch * wl.chunk / (ms / 1e3),
                     roofline={"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
                               "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None,

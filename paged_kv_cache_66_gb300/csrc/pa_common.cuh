@@ -110,15 +110,31 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// As mbar_try_wait, with a suspend-time hint: a thread whose phase is not complete may sleep up
+// to `ns` nanoseconds (it resumes when the phase completes) before the test gives up.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` with a time limit (default 1 s).  Returns
 // false on timeout; the caller records PA_DEVERR_TIMEOUT and winds down.
+// suspend_ns > 0: each retry may sleep that long (fewer issue slots spent polling; the clock is
+// then read after every retry).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint64_t limit_ns = 1000000000ull) {
+                                                  uint64_t limit_ns = 1000000000ull, uint32_t suspend_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        if (suspend_ns ? mbar_try_wait_for(bar, parity, suspend_ns) : mbar_try_wait(bar, parity)) return true;
+        if ((suspend_ns != 0 || (it & 255u) == 0) && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -85,6 +85,13 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
         : "f"(a0), "f"(a1));
 }
 
+// The kernels' bounded waits (1 s) with a 2 us suspend hint per retry: the warps of one
+// softmax group sleep while the other group works instead of taking issue slots to poll
+// (measured +1.4 % at D = 64, +0.3 % at D = 128; the decode kernels gained nothing from it)
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_bounded(bar, parity, 1000000000ull, 2000u);
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
                 if (lane == 0 && ok) {
                     // the stage's previous tile is released after both its MMAs consumed it, which
                     // needs this tile's predecessors' copies: at most one phase ahead
-                    if (!mbar_wait_bounded(&kv_empty[st], ((j / STAGES) & 1) ^ 1)) {
+                    if (!tc05::wait_bounded(&kv_empty[st], ((j / STAGES) & 1) ^ 1)) {
                         flag_error(p.err, PA_DEVERR_TIMEOUT);
                         ok = false;
                     } else {
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
             constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
             // Q in tensor memory: written by the softmax threads (tcgen05.st) before q_full
-            bool ok = mbar_wait_bounded(q_full, 0);
+            bool ok = tc05::wait_bounded(q_full, 0);
             tc05::fence_after();
             // descriptors formed once; an operand at byte offset o from a base has the base's
             // descriptor plus o / 16 (shared addresses stay below 2^18: no carry out of the field)
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             // kv_full of tile j cannot complete another phase before kv_empty of tile j is
             // committed (after its P . V, below), so each wait's parity is unambiguous
             if (ok && n_kv > 0) {
-                ok = mbar_wait_bounded(&kv_full[0], 0);
+                ok = tc05::wait_bounded(&kv_full[0], 0);
                 if (ok) {
                     tc05::fence_after();
                     issue_s(0);
@@ -192,13 +192,13 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (j + 1 < n_kv) {
-                    ok = mbar_wait_bounded(&kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1);
+                    ok = tc05::wait_bounded(&kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1);
                     if (!ok) break;
                     tc05::fence_after();
                     issue_s(j + 1);  // its S buffer held P(j-1), whose P . V was issued before
                 }
                 // P(j + NSB) needs S(j + NSB), issued after this P . V: at most one phase ahead
-                ok = mbar_wait_bounded(&p_full[j % NSB], (j / NSB) & 1);
+                ok = tc05::wait_bounded(&p_full[j % NSB], (j / NSB) & 1);
                 if (!ok) break;
                 tc05::fence_after();
                 const int st = j % STAGES;
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
         // decisions that guard a tcgen05.ld / st are warp-uniform (those are .sync.aligned).
         // Neither barrier can run two phases ahead: tile j + STAGES is loaded, and S(j + NSB)
         // issued, only after this thread's P_j has been consumed
-        const bool got = mbar_wait_bounded(&kv_full[st], (j / STAGES) & 1) && mbar_wait_bounded(&s_full[sb], (j / NSB) & 1);
+        const bool got = tc05::wait_bounded(&kv_full[st], (j / STAGES) & 1) && tc05::wait_bounded(&s_full[sb], (j / NSB) & 1);
         if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
         if (j > 0 && __any_sync(0xffffffffu, scale_o)) {
             // o_ready counts the P . V launches in order: the one of tile j needs this thread's P_j,
             // and the one of tile j - 2 completed before S(j) (issued after it)
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_ready, (j - 1) & 1))) {
+            if (!__all_sync(0xffffffffu, tc05::wait_bounded(o_ready, (j - 1) & 1))) {
                 ok = false;
                 break;
             }
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
     }
     griddep_launch_dependents();
     const bool all_ok = tc05::bar_and(2, C::NSW * 32, ok);
-    const bool done = all_ok && mbar_wait_bounded(o_final, 0);
+    const bool done = all_ok && tc05::wait_bounded(o_final, 0);
     if (__all_sync(0xffffffffu, done)) {
         tc05::fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;

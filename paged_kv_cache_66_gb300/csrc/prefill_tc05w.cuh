@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                 if (lane == 0 && ok) {
                     // the slot's previous tile (j - SLOTS) is released after its MMAs have consumed it,
                     // which needs this tile's predecessor copies: at most one phase ahead
-                    if (!mbar_wait_bounded(&empty[sl], ((j / SLOTS) & 1) ^ 1)) {
+                    if (!tc05::wait_bounded(&empty[sl], ((j / SLOTS) & 1) ^ 1)) {
                         flag_error(p.err, PA_DEVERR_TIMEOUT);
                         ok = false;
                     } else {
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
             constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
-            bool ok = mbar_wait_bounded(q_full, 0);
+            bool ok = tc05::wait_bounded(q_full, 0);
             tc05::fence_after();
             // descriptors formed once; an operand at byte offset o from a base has the base's
             // descriptor plus o / 16 (shared addresses stay below 2^18: no carry out of the field)
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
             // k_full / v_full of tile j cannot complete the next phase of their slot before k_empty /
             // v_empty of tile j is committed (below), so each wait's parity is unambiguous
             if (ok && n_kv > 0) {
-                ok = mbar_wait_bounded(&k_full[0], 0);
+                ok = tc05::wait_bounded(&k_full[0], 0);
                 if (ok) {
                     tc05::fence_after();
                     issue_s(0, 0);
@@ -241,28 +241,28 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int sl = j % SLOTS;
                 const bool more = j + 1 < n_kv;
-                ok = mbar_wait_bounded(&v_full[sl], (j / SLOTS) & 1);
+                ok = tc05::wait_bounded(&v_full[sl], (j / SLOTS) & 1);
                 // P_X(j+1) needs S_X(j+1), issued below after both waits of P_Xj: each half's
                 // p_full is at most one phase ahead
-                ok = ok && mbar_wait_bounded(&p_full[0], j & 1);
+                ok = ok && tc05::wait_bounded(&p_full[0], j & 1);
                 if (!ok) break;
                 tc05::fence_after();
                 issue_pv(0, j, 0);
-                ok = mbar_wait_bounded(&p_full[1], j & 1);
+                ok = tc05::wait_bounded(&p_full[1], j & 1);
                 if (!ok) break;
                 tc05::fence_after();
                 issue_pv(0, j, 1);
                 if (more) {
-                    ok = mbar_wait_bounded(&k_full[(j + 1) % SLOTS], ((j + 1) / SLOTS) & 1);
+                    ok = tc05::wait_bounded(&k_full[(j + 1) % SLOTS], ((j + 1) / SLOTS) & 1);
                     if (!ok) break;
                     tc05::fence_after();
                     issue_s(0, j + 1);  // after P_A(j) . V_j on the pipe: overwrites P_A(j) in S_A
                 }
-                ok = mbar_wait_bounded(&p_full[2], j & 1);
+                ok = tc05::wait_bounded(&p_full[2], j & 1);
                 if (!ok) break;
                 tc05::fence_after();
                 issue_pv(1, j, 0);
-                ok = mbar_wait_bounded(&p_full[3], j & 1);
+                ok = tc05::wait_bounded(&p_full[3], j & 1);
                 if (!ok) break;
                 tc05::fence_after();
                 issue_pv(1, j, 1);
@@ -325,8 +325,8 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
         // decisions that guard a tcgen05.ld / st are warp-uniform (those are .sync.aligned).
         // Neither barrier can run two phases ahead: V of tile j + SLOTS is loaded, and S_X(j + 1)
         // issued, only after this thread's P_Xj has been consumed
-        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&v_full[sl], (j / SLOTS) & 1) &&
-                                                     mbar_wait_bounded(&s_full[X], j & 1));
+        const bool got = __all_sync(0xffffffffu, tc05::wait_bounded(&v_full[sl], (j / SLOTS) & 1) &&
+                                                     tc05::wait_bounded(&s_full[X], j & 1));
         const int key0 = j * BN;
         int okmask = 0;
         bool interior = false;
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
     }
     griddep_launch_dependents();
     const bool all_ok = tc05::bar_and(2, C::NSW * 32, ok);
-    const bool done = all_ok && mbar_wait_bounded(o_final, 0);
+    const bool done = all_ok && tc05::wait_bounded(o_final, 0);
     // the row sum: this half's share plus the partner's (every softmax thread passed the barrier
     // above, so the exchange below is reached by the whole group)
     xl[(X * 2 + hh) * 128 + r] = l;
