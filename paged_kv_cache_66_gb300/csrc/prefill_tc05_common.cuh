@@ -147,23 +147,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// (2^x0, 2^x1) with one MUFU instruction for both (ex2.approx.f16x2).  The exponents are
-// rounded to f16 first (half an ulp: 2^-11 relative), which moves 2^x by ln 2 * 2^-11 * |x|
-// relative: at most 0.034 % for |x| < 1 (the keys near the row max, which carry the weight),
-// 0.14 % for 4 <= |x| < 8 and 0.27 % for 8 <= |x| < 16 (weights of 2^-4 and below, or up to
-// 2^8 while the lazy reference lags: the softmax keeps every exponent at or below 8).  The
-// results are f16.  Returns the pair as f16x2 bits (x0 in the low half) and, exactly, as two
-// floats.
-__device__ __forceinline__ uint32_t exp2_h2(float x0, float x1, float& e0, float& e1) {
-    uint32_t h, r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
-    asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(h));
-    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-        : "=f"(e0), "=f"(e1)
-        : "r"(r));
-    return r;
-}
-
 // barrier `id` over `count` threads that also ANDs `pred` over them
 __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
     uint32_t out;

@@ -423,15 +423,9 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                     const int c = qq * 32 + hv * 16 + 2 * i;
                     float x0, x1;
                     tc05::fma2(x0, x1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), mul, -ms);
-                    float e0, e1;
-                    if constexpr (D == 128) {
-                        // both exponentials in one MUFU instruction (f16 precision, then P's own
-                        // rounding); P is repacked from the exact f32 copies
-                        tc05::exp2_h2(x0, x1, e0, e1);
-                    } else {
-                        e0 = tc05::fast_exp2(x0);
-                        e1 = tc05::fast_exp2(x1);
-                    }
+                    // fp32 exponentials (with the 8-word stores, the f16x2 form -- one MUFU op per
+                    // pair, three conversions more -- measured slower at every share of the pairs)
+                    const float e0 = tc05::fast_exp2(x0), e1 = tc05::fast_exp2(x1);
                     pw[i] = pack2<T>(e0, e1);
                     tc05::add2(ls[(i & 1) * 2], ls[(i & 1) * 2 + 1], e0, e1);
                 }
