@@ -127,7 +127,8 @@ size_t pa_decode_workspace_size(int batch, int num_q_heads, int head_dim, int ma
  *   k_pool,v_pool [num_blocks, Hkv, b, D] in `dtype`.
  *   block_tables  [B, max_blocks] int32; row s lists the physical blocks of
  *                 sequence s in logical order; entries past ceil(L_s / b) are
- *                 never read (pad with anything).
+ *                 never used (the whole row must be readable: a partition's
+ *                 entries may be loaded before L_s is known; pad with anything).
  *   seq_lens      [B] int32; L_s >= 1 tokens of history (the token appended
  *                 this step included).  L_s = 0 writes a zero row.
  *   scale         multiplies q . k (the pages use 1 / sqrt(D)).
