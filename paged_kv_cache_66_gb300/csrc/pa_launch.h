@@ -88,6 +88,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // 2-D map over a pool viewed as `rows` rows of `d` elements: boxes of 128 bytes x box_rows rows,
 // 128-byte swizzle
 bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes, int box_rows = 16);
+// Tensor map over a packed 16-bit query tensor [total_q, hq, d] whose box is one 128-row query tile
+// of the prefill kernels: 64 dims x g heads x 128 / g tokens (rows token-major, the g heads of a token
+// side by side), 128-byte swizzle, zeros past total_q.  q 16-byte aligned.
+bool encode_q_tmap(CUtensorMap* map, const void* q, int total_q, int hq, int d, int g);
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_pool, void* v_pool, const int64_t* slots,
                              int64_t num_tokens, int64_t num_blocks, int hkv, int row_bytes, int block_size,

@@ -12,7 +12,9 @@ template <typename T, int D, int G>
 cudaError_t launch_prefill_path(const PrefillParams& p, const CUtensorMap& km, const CUtensorMap& vm, int max_q,
                                 cudaStream_t stream) {
     if constexpr (D <= 128) {
-        return launch_prefill_tc05w<T, D, G>(p, km, vm, max_q, stream);
+        CUtensorMap qm;
+        if (!encode_q_tmap(&qm, p.q, p.total_q, p.hq, D, G)) return cudaErrorInvalidValue;
+        return launch_prefill_tc05w<T, D, G>(p, km, vm, qm, max_q, stream);
     } else {
         return launch_prefill_tc05d<T, G>(p, km, vm, max_q, stream);
     }

@@ -13,6 +13,16 @@
 #include "decode_mma.cuh"
 
 namespace pa {
+
+// 3-D tiled TMA load (box of the map at element coordinates x, y, z), completing on `bar`
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 namespace tc05 {
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -112,6 +122,15 @@ __device__ __forceinline__ void st8(uint32_t addr, const uint32_t* r) {
                  : "memory");
 }
 
+__device__ __forceinline__ void ld16(uint32_t addr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(addr));
+}
+
 __device__ __forceinline__ void st32(uint32_t addr, const uint32_t* r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -138,6 +157,21 @@ __device__ __forceinline__ bool test_wait(uint64_t* bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// Multiply N columns of this warp's tensor-memory lanes, starting at `addr`, by `a` (warp-uniform
+// call).  Kept out of line: the rare rescale of O then costs the softmax loop no registers.
+template <int N>
+__device__ __noinline__ void scale_tmem_cols(uint32_t addr, float a) {
+#pragma unroll
+    for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t o[32];
+        ld32(addr + c0, o);
+        wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+        st32(addr + c0, o);
+    }
 }
 
 // 2^x by the MUFU approximation (relative error ~2^-22; 2^-inf = 0)
