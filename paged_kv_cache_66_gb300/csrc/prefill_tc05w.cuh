@@ -102,13 +102,19 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
     griddep_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Work units: (query tile pair, KV head, sequence) with the tile pair fastest, the pairs with the
-    // most keys first; CTA c takes units c, c + gridDim.x, ...  The CTAs at work at any time hold all
-    // tile pairs of a few (sequence, KV head)s, which read the same K/V blocks (one DRAM read, the rest
-    // from L2).  Every role walks the same units and skips the same ones, so the barrier phases below
-    // count the same K/V tiles and units everywhere.
+    // most keys first; in round r CTA c takes unit r * grid + c (r even) or r * grid + grid - 1 - c
+    // (r odd).  The CTAs at work at any time hold all tile pairs of a few (sequence, KV head)s, which
+    // read the same K/V blocks (one DRAM read, the rest from L2).  Every role walks the same units and
+    // skips the same ones, so the barrier phases below count the same K/V tiles and units everywhere.
     const int n_units = q_tiles * p.hkv * p.batch;  // < 2^31 (the launcher checks)
     struct Unit {
         int s, kvh, q0, Cq, L, base, tok0, n_kv;
+    };
+    // the unit of this CTA's round r: rounds alternate direction over the CTAs (a snake), which
+    // evens out the per-CTA work when the tile pairs' key counts grow with their index
+    auto unit_of = [&](int rnd) -> int {
+        return rnd * static_cast<int>(gridDim.x) +
+               ((rnd & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
     };
     // n_kv = 0: a unit with no rows (past its sequence's chunk, or an inconsistent sequence)
     auto unit_at = [&](int u) -> Unit {
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
         const CUtensorMap* map = is_v ? &vmap : &kmap;
         bool ok = true;
         int jg = 0, nu = 0;  // K/V tiles and units of this CTA so far
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int rnd = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++rnd)) {
             const Unit w = unit_at(u);
             if (w.n_kv == 0) continue;
             if (!is_v) {
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
             // v_empty of tile g is committed (below), so each wait's parity is unambiguous.
             bool ok = true;
             int jg = 0, nu = 0;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            for (int rnd = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++rnd)) {
                 const Unit w = unit_at(u);
                 if (w.n_kv == 0) continue;
                 const int n_kv = w.n_kv;
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     int jg = 0, nu = 0;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int rnd = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++rnd)) {
         const Unit w = unit_at(u);
         if (w.n_kv == 0) continue;
         const int n_kv = w.n_kv, L = w.L;
