@@ -204,3 +204,35 @@ def test_prefill_bench_workload_sampled_rows(api, dtype, head_dim):
         Vh = oatt.gather_history(V, wl.tables()[s], pos + 1, wl.b)
         want = oprefill.prefill_attention(qc[s * wl.chunk + r][None], Kh, Vh, wl.scale)[0]
         assert np.abs(got[s * wl.chunk + r] - want).max() <= tol
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_prefill_many_units_per_cta_ragged(api, D):
+    """More work units than SMs, so each persistent CTA walks many of them: chunks of 0 to 512
+    rows (many units empty and skipped), one inconsistent sequence in the middle (flagged, its
+    rows left unwritten), and sampled rows of every other sequence against the oracle."""
+    from oracle import attention as oatt
+    Hq, Hkv, b, dtype = 32, 8, 16, torch.bfloat16
+    rng = np.random.default_rng(77 + D)
+    chunks = [int(c) for c in rng.choice([0, 1, 37, 128, 256, 300, 512], size=24)]
+    bad = 7
+    chunks[5], chunks[11], chunks[bad] = 512, 0, 37
+    lengths = [c + int(h) for c, h in zip(chunks, rng.integers(1, 300, size=24))]
+    K, V, q, tables, lens, qstart = _setup(lengths, chunks, Hq, Hkv, D, b, dtype, seed=500 + D)
+    lens[bad] = chunks[bad] - 1                           # a chunk longer than its sequence
+    got = _run(api, K, V, q, tables, lens, qstart, 1 / math.sqrt(D), max_q=max(chunks))
+    assert api.pa_get_device_error() == 4                 # PA_DEVERR_SEQLEN, and nothing else
+    qs = qstart.tolist()
+    assert torch.isnan(got[qs[bad]:qs[bad + 1]]).all()
+    Kd, Vd, qd, gd = K.double(), V.double(), q.double().numpy(), got.double().numpy()
+    for s in range(24):
+        C = qs[s + 1] - qs[s]
+        if s == bad or C == 0:
+            continue
+        L = int(lens[s])
+        for r in sorted({0, C // 2, C - 1}):
+            pos = L - C + r
+            Kh = oatt.gather_history(Kd, tables[s].tolist(), pos + 1, b)
+            Vh = oatt.gather_history(Vd, tables[s].tolist(), pos + 1, b)
+            want = oprefill.prefill_attention(qd[qs[s] + r][None], Kh, Vh, 1 / math.sqrt(D))[0]
+            _check(gd[qs[s] + r][None], want[None], Vh, dtype, [pos + 1])
