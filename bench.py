@@ -745,7 +745,7 @@ def run_op(args, local):
                     tokens_per_s=wl.batch * wl.chunk / (ms / 1e3),
                     roofline={"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
                               "alg_flops_per_launch": flops, "peak_kind": tkind, "traffic": None,
-                              "kernel": "pa_prefill (tcgen05, 128-key tiles)" if wl.D <= 128
+                              "kernel": "pa_prefill (tcgen05, persistent CTAs, 128-key tiles)" if wl.D <= 128
                               else "pa_prefill (tcgen05, Q in tensor memory)"},
                     clocks={k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
                     gpu_launches=K)
