@@ -139,6 +139,16 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
         return w;
     };
 
+    // the next unit with rows at or after round `rnd` (rnd is advanced past it; n_kv = 0: none)
+    auto next_unit = [&](int& rnd) -> Unit {
+        for (int u = unit_of(rnd); u < n_units; u = unit_of(rnd)) {
+            ++rnd;
+            const Unit w = unit_at(u);
+            if (w.n_kv > 0) return w;
+        }
+        return Unit{};
+    };
+
     if (tid == 0) {
 #pragma unroll
         for (int i = 0; i < SLOTS; ++i) {
@@ -205,6 +215,19 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                if (lane == 0) {
+                    // the next unit's Q tiles into L2 now, so that its TMA load, issued only once this
+                    // unit's score MMAs are done, finds them there
+                    int r2 = rnd + 1;
+                    const Unit w2 = next_unit(r2);
+                    if (w2.n_kv > 0) {
+#pragma unroll
+                        for (int X = 0; X < 2; ++X)
+#pragma unroll
+                            for (int bx = 0; bx < NBOX; ++bx)
+                                tma_prefetch_3d(&qmap, bx * 64, w2.kvh * G, w2.q0 + w2.tok0 + X * QTX);
+                    }
+                }
             }
             const int32_t* trow = p.block_tables + static_cast<size_t>(w.s) * p.max_blocks;
             const int n_sub = w.n_kv * SUB;
@@ -297,10 +320,12 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
             // v_empty of tile g is committed (below), so each wait's parity is unambiguous.
             bool ok = true;
             int jg = 0, nu = 0;
-            for (int rnd = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++rnd)) {
-                const Unit w = unit_at(u);
-                if (w.n_kv == 0) continue;
-                const int n_kv = w.n_kv;
+            // the next unit is found while the current one runs (its loads off the unit boundary)
+            int rnd_is = 0;
+            Unit w_is = next_unit(rnd_is);
+            while (w_is.n_kv > 0 && ok) {
+                const Unit w_after = next_unit(rnd_is);
+                const int n_kv = w_is.n_kv;
                 ok = tc05::wait_bounded(q_full, nu & 1) && tc05::wait_bounded(&k_full[jg % SLOTS], (jg / SLOTS) & 1);
                 if (!ok) break;
                 tc05::fence_after();
@@ -347,6 +372,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
                 tc05::commit(o_final);
                 jg += n_kv;
                 ++nu;
+                w_is = w_after;
             }
             if (!ok) flag_error(p.err, PA_DEVERR_TIMEOUT);
         }
@@ -372,6 +398,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
     float* xl = xmax + 2 * 2 * 2 * 128;                          // [X][half][row]
     const int gbar = 3 + X;                                      // the group's named barrier (256 threads)
     const float sl2 = p.scale_log2;
+    const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;  // rows are 2 D bytes apart
     bool ok = true;
     int jg = 0, nu = 0;
     for (int rnd = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++rnd)) {
@@ -505,6 +532,7 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
             ok = false;
             break;
         }
+
         // the row sum: this half's share plus the partner's; xl is written again only after every
         // softmax thread has passed the next unit's first barrier above
         xl[(X * 2 + hh) * 128 + r] = l;
@@ -521,14 +549,17 @@ __global__ void __launch_bounds__(Tc05wCfg<D_>::THREADS, 1)
             tc05::ld16(o_addr + c0, o);
             tc05::wait_ld();
             if (orow_off >= 0) {
+                uint32_t pw[8];
 #pragma unroll
-                for (int i = 0; i < 16; i += 8) {
-                    uint4 v4;
-                    v4.x = pack2<T>(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
-                    v4.y = pack2<T>(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-                    v4.z = pack2<T>(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
-                    v4.w = pack2<T>(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
-                    *reinterpret_cast<uint4*>(orow + c0 + i) = v4;
+                for (int i = 0; i < 8; ++i)
+                    pw[i] = pack2<T>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                // lanes hold different rows: a 32-byte store per lane writes whole sectors, half as
+                // many L2 transactions as 16-byte ones (the epilogue's stores were its whole cost)
+                if (out32) {
+                    st_global_v8(orow + c0, pw);
+                } else {
+                    *reinterpret_cast<uint4*>(orow + c0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    *reinterpret_cast<uint4*>(orow + c0 + 8) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
                 }
             }
         }
