@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
     if (__all_sync(0xffffffffu, done)) {
         tc05::fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;  // rows are 2 D bytes apart
         T* orow = static_cast<T*>(p.out) + (static_cast<size_t>(q0 + (valid ? tok : 0)) * p.hq + head) * D;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -380,13 +381,18 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             tc05::wait_ld();
             if (valid) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 u;
-                    u.x = pack2<T>(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
-                    u.y = pack2<T>(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-                    u.z = pack2<T>(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
-                    u.w = pack2<T>(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
-                    *reinterpret_cast<uint4*>(orow + c0 + i) = u;
+                for (int i = 0; i < 32; i += 16) {
+                    uint32_t pw[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        pw[k] = pack2<T>(__uint_as_float(o[i + 2 * k]) * inv, __uint_as_float(o[i + 2 * k + 1]) * inv);
+                    // lanes hold different rows: 32 bytes per lane write whole sectors
+                    if (out32) {
+                        st_global_v8(orow + c0 + i, pw);
+                    } else {
+                        *reinterpret_cast<uint4*>(orow + c0 + i) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        *reinterpret_cast<uint4*>(orow + c0 + i + 8) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                    }
                 }
             }
         }
