@@ -631,6 +631,7 @@ cudaError_t launch_mma(const DecodeParams& p_in, const CUtensorMap& kmap, const 
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, decode_partition_mma<T, PE, D, G>, C::NW * 32,
                                                               C::smem_bytes(entries, 2));
         if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
         cached_hpc = occ2 >= occ1 ? 2 : 1;
         cached_entries = entries;
     }
