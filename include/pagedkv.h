@@ -270,8 +270,11 @@ pa_status pa_decode_fp8(void* out, const void* q, pa_dtype q_dtype, const void* 
  *                 (pa_kv_append).
  *   k_pool, v_pool, block_tables, max_blocks, num_blocks, block_size: as for
  *                 pa_decode.
- *   max_query_len the largest C of the batch (sizes the grid; a smaller
- *                 value leaves the rows past it unwritten).
+ *   max_query_len the largest C of the batch: it sizes the work, units of
+ *                 256 (D <= 128) or 128 (D = 256) query rows of one KV head
+ *                 (a row = a chunk token x a query head of the group); a
+ *                 smaller value leaves the rows past it unwritten.  At
+ *                 D <= 128 one persistent CTA per SM walks the units.
  *   scale         multiplies q . k (typically 1/sqrt(D)).
  *
  * Output rows are rounded once from fp32 to `dtype`.  Tensor-core kernel
