@@ -325,7 +325,7 @@ class L2Flush:
 
 
 def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=True, flush_l2=False,
-                    min_seconds=0.0):
+                    min_seconds=0.0, auto_partition=False):
     """Time ``steps`` decode steps of ``wl`` on the device, inputs resident in HBM.
 
     The host plans of every step are made and uploaded first.  Without
@@ -344,7 +344,7 @@ def _measure_device(wl, steps, warmup, dev, ws, kv="native", partition=0, fused=
     from paged_kv_cache_66_gb300 import api
     from paged_kv_cache_66_gb300.replay import Replay
 
-    rp = Replay(wl, device=dev, kv=kv, partition_tokens=partition or None, fused=fused)
+    rp = Replay(wl, device=dev, kv=kv, partition_tokens=0 if auto_partition else (partition or None), fused=fused)
     rp.run_setup()
     torch.cuda.synchronize()
     total_steps = warmup + steps
@@ -435,7 +435,9 @@ SECONDARY = [
     {"config": 5, "combo": (64, 8, 16, "bf16"), "kv": "native"},
     {"config": 5, "combo": (128, 8, 32, "bf16"), "kv": "native"},
     {"config": 2, "kv": "native"},
-    {"config": 3, "kv": "fp8"},
+    # E4M3 pools take the library's automatic partition size (2048 tokens here): config 3 states
+    # its 512-token split for 16-bit pools, where a token carries twice the bytes
+    {"config": 3, "kv": "fp8", "auto_partition": True},
 ]
 L2_BYTES = 129 << 20
 
@@ -452,11 +454,14 @@ def _secondary(spec, steps, warmup, dev, ws, peak):
     wl = _workload(spec["config"], warmup + steps + 1, spec.get("combo"))
     kv = spec["kv"]
     small = _history_bytes(wl, 1 if kv == "fp8" else wl.elt) < 4 * L2_BYTES
-    rp, m = _measure_device(wl, steps, warmup, dev, ws, kv=kv, flush_l2=small, min_seconds=0.5)
+    auto = spec.get("auto_partition", False)
+    rp, m = _measure_device(wl, steps, warmup, dev, ws, kv=kv, flush_l2=small, min_seconds=0.5,
+                            auto_partition=auto)
     steps = m["steps"]
     ms = m["dev_ms_max"] / steps
     entry = {
         "workload": wl.name, "kv_cache": "e4m3" if kv == "fp8" else wl.dtype, "batch": m["B"],
+        "partition_tokens": "automatic" if auto or not wl.partition_tokens else wl.partition_tokens,
         "layers": m["nL"], "steps": steps, "planned_steps": m["planned_steps"], "warmup": warmup,
         "ms_per_step": ms,
         "effective_kv_gbs": m["kv_bytes"] / (m["dev_ms_max"] / 1e3) / 1e9,
@@ -492,7 +497,9 @@ def run_ours(args, ws, rank, local):
     wl = _workload(args.config, total_steps + args.steps + 1, args.combo)
     if args.layers:
         wl.layers = min(wl.layers, args.layers)
+    fp8_auto = args.kv == "fp8" and not args.partition  # E4M3 pools: the library's automatic size
     rp, m = _measure_device(wl, args.steps, args.warmup, dev, ws, kv=args.kv, partition=args.partition,
+                            auto_partition=fp8_auto,
                             fused=not args.unfused, flush_l2=args.flush_l2)
     traffic = _profiled_traffic(_launch_key(args, wl, rp))
     plans, nL, B = m["plans"], m["nL"], m["B"]
@@ -525,7 +532,8 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": wl.name, "batch": B, "context": int(np.max(plans[0].lens)), "layers": nL,
                    "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.b,
-                   "partition_tokens": wl.partition_tokens if not args.partition else args.partition,
+                   "partition_tokens": ("automatic" if fp8_auto else
+                                        wl.partition_tokens if not args.partition else args.partition),
                    "kv_cache": "e4m3" if args.kv == "fp8" else wl.dtype,
                    "l2": (L2_FLUSH_DOC + "; each step timed by its own events" if args.flush_l2
                           else "inputs larger than L2 (no flush needed)"),

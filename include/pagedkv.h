@@ -236,7 +236,11 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_pool, const 
  *   history, with q used in f16 (exact for bf16 values in f16's normal range)
  *   and fp32 accumulation.  Tensor-core kernel only: D in {64, 128, 256}, Hq/Hkv in
  *   {1, 2, 4, 8}, b a multiple of 16, num_blocks * Hkv * b < 2^31 (else
- *   PA_ERR_UNSUPPORTED).  Workspace as for pa_decode.
+ *   PA_ERR_UNSUPPORTED).  Workspace as for pa_decode.  partition_tokens = 0
+ *   takes the automatic size for E4M3 pools: 2048 tokens (a token carries
+ *   half the bytes), halved down to 128 while the launch would have fewer
+ *   than ~2 units per SM; it is never smaller than pa_decode's automatic
+ *   size, so pa_decode_workspace_size(..., 0) bytes always suffice.
  */
 pa_status pa_kv_append_fp8(const void* k, const void* v, pa_dtype in_dtype, void* k_pool, void* v_pool,
                            const float* k_scale, const float* v_scale, const int64_t* slot_mapping,

@@ -112,6 +112,7 @@ FP8_CASES = [
     (32, 4, 64, 16, [3, 300], 0),                        # G = 8
     (32, 8, 128, 48, [47, 49, 1000], 480),               # three 16-token tiles per block
     (16, 4, 64, 80, [79, 81, 900], 400),                 # five tiles per block, token-pair lines
+    (32, 8, 128, 16, [5000, 2049, 10], 0),               # the automatic E4M3 size: 2048-token partitions
 ]
 
 
