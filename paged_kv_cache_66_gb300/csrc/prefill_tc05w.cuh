@@ -14,7 +14,7 @@
 //
 // A unit of work is 256 query rows of one KV head, two 128-row tiles X = A, B that
 // share every 128-key K/V tile j.  The kernel is persistent: one CTA per SM walks
-// its units back to back (CTA c takes units c, c + grid, ...), its producers running
+// its units back to back (dealt round by round in a snake over the CTAs), its producers running
 // on into the next unit's K/V tiles, the next unit's Q tiles loaded by TMA as soon as
 // the unit before has no score MMA left, and tensor memory allocated once.  Each
 // unit ends with its O read, normalised and stored by the softmax warps before they
