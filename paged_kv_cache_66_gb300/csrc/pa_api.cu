@@ -134,6 +134,20 @@ bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_pool_tmap_slices(CUtensorMap* map, const void* pool, uint64_t rows, int d, int box_rows) {
+    auto enc = encoder();
+    if (!enc || d % 64 != 0 || d / 64 > 256 || box_rows <= 0 || box_rows > 256) return false;
+    // dims (element in the slice, row, slice): the row's stride is the whole row, the slice's 128 B,
+    // so one box lands as [slice][box_rows rows][128 B], each slice its own run of 128-byte rows
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(d / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(d / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_q_tmap(CUtensorMap* map, const void* q, int total_q, int hq, int d, int g) {
     auto enc = encoder();
     if (!enc || g <= 0 || 128 % g != 0 || d % 64 != 0) return false;

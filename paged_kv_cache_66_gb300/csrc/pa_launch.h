@@ -88,6 +88,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // 2-D map over a pool viewed as `rows` rows of `d` elements: boxes of 128 bytes x box_rows rows,
 // 128-byte swizzle
 bool encode_pool_tmap(CUtensorMap* map, const void* pool, uint64_t rows, int d, int elt_bytes, int box_rows = 16);
+// 3-D map over a 16-bit pool viewed as `rows` rows of `d` elements, in which one box is box_rows
+// rows of every 64-element (128-byte) slice of the row: it lands as d / 64 runs of box_rows
+// 128-byte rows, one run per slice, with the 128-byte swizzle.  d a multiple of 64.
+bool encode_pool_tmap_slices(CUtensorMap* map, const void* pool, uint64_t rows, int d, int box_rows);
 // Tensor map over a packed 16-bit query tensor [total_q, hq, d] whose box is one 128-row query tile
 // of the prefill kernels: 64 dims x g heads x 128 / g tokens (rows token-major, the g heads of a token
 // side by side), 128-byte swizzle, zeros past total_q.  q 16-byte aligned.

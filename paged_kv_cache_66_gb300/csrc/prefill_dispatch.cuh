@@ -38,8 +38,12 @@ cudaError_t dispatch_prefill(const PrefillParams& p, const void* k_pool, const v
     const uint64_t rows = static_cast<uint64_t>(p.num_blocks) * p.hkv * p.block_size;
     if (rows >= (1ull << 31)) return cudaErrorNotSupported;
     CUtensorMap km, vm;
-    if (!encode_pool_tmap(&km, k_pool, rows, d, 2) || !encode_pool_tmap(&vm, v_pool, rows, d, 2))
-        return cudaErrorInvalidValue;
+    // D = 256: one box spans the row's four 64-dim slices (8 rows of K, 16 of V): 12 copies per
+    // 64-key tile instead of 32; D <= 128: boxes of 16 rows x 128 bytes
+    const bool ok = d == 256 ? encode_pool_tmap_slices(&km, k_pool, rows, d, 8) &&
+                                   encode_pool_tmap_slices(&vm, v_pool, rows, d, 16)
+                             : encode_pool_tmap(&km, k_pool, rows, d, 2) && encode_pool_tmap(&vm, v_pool, rows, d, 2);
+    if (!ok) return cudaErrorInvalidValue;
     switch (d) {
         case 64: return dispatch_prefill_group<T, 64>(p, km, vm, max_q, stream);
         case 128: return dispatch_prefill_group<T, 128>(p, km, vm, max_q, stream);

@@ -7,7 +7,11 @@
 // columns, fp32), the query tile Q as the A operand of the score MMAs (128
 // columns, two 16-bit values per column, written once by the softmax threads)
 // and two 64-column S buffers; shared memory then holds only the K/V ring, three
-// stages of 64 keys (64 KiB each).  Per 64-key tile j:
+// stages of 64 keys (64 KiB each).  A K/V copy takes every 64-dim slice of its
+// rows at once (a 3-D box: 8 rows of K, 16 of V), so the 64-key tile is 12 TMA
+// copies: K as eight 8-key groups of [slice][8 rows][128 B] (4 KiB apart, the
+// score MMA's 8-row step), V as four 16-key sub-tiles of [slice][16 rows][128 B]
+// (8 KiB apart, one P . V K-step each; slices 2 KiB apart).  Per 64-key tile j:
 //   S_j = Q . K_j^T   tcgen05.mma M=128 N=64, A = Q (tensor memory), B = K_j (smem, K-major)
 //   softmax           one thread per row: tcgen05.ld of its 64 scores, causal mask, running
 //                     max, P_j = 2^(s - m) rounded to the dtype over the first half of S_j
@@ -30,6 +34,8 @@ struct Tc05dCfg {
     static constexpr int NBOX = D / 64;              // 64-dim (128-byte) boxes per row
     static constexpr int KV_BOX = BN * 128;          // 64 keys x 128 B
     static constexpr int K_BYTES = NBOX * KV_BOX;    // 32 KiB
+    static constexpr int KG_BYTES = 8 * NBOX * 128;  // one 8-key group of K, all slices (4 KiB)
+    static constexpr int VS_BYTES = 16 * NBOX * 128; // one 16-key sub-tile of V, all slices (8 KiB)
     static constexpr int STAGE_BYTES = 2 * K_BYTES;  // K then V
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
     // kv_full, kv_empty [STAGES]; s_full, p_full [NSB]; o_ready; o_final; q_full
@@ -144,14 +150,14 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                // lanes 0-3 issue the copies of sub-tiles 0-3 side by side
+                // lanes 0-3 issue the copies of sub-tiles 0-3 side by side: K as its two 8-key
+                // groups, V whole
                 if (ok && lane < 4 && my_row >= 0) {
-                    unsigned char* kd = smem + st * C::STAGE_BYTES + lane * 2048;
-#pragma unroll
-                    for (int bx = 0; bx < NBOX; ++bx) {
-                        tma_load_2d(kd + bx * C::KV_BOX, &kmap, bx * 64, my_row, &kv_full[st]);
-                        tma_load_2d(kd + C::K_BYTES + bx * C::KV_BOX, &vmap, bx * 64, my_row, &kv_full[st]);
-                    }
+                    unsigned char* kd = smem + st * C::STAGE_BYTES + lane * 2 * C::KG_BYTES;
+                    tma_load_3d(kd, &kmap, 0, my_row, 0, &kv_full[st]);
+                    tma_load_3d(kd + C::KG_BYTES, &kmap, 0, my_row + 8, 0, &kv_full[st]);
+                    tma_load_3d(smem + st * C::STAGE_BYTES + C::K_BYTES + lane * C::VS_BYTES, &vmap, 0, my_row, 0,
+                                &kv_full[st]);
                 }
                 __syncwarp();
             }
@@ -168,15 +174,16 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             bool ok = tc05::wait_bounded(q_full, 0);
             tc05::fence_after();
             // descriptors formed once; an operand at byte offset o from a base has the base's
-            // descriptor plus o / 16 (shared addresses stay below 2^18: no carry out of the field)
-            const uint64_t k_desc = tc05::sdesc(sbase, 16, 1024);
-            const uint64_t v_desc = tc05::sdesc(sbase + C::K_BYTES, C::KV_BOX, 1024);
+            // descriptor plus o / 16 (shared addresses stay below 2^18: no carry out of the field).
+            // K: 8-key groups KG_BYTES apart; V: 8-key groups 1 KiB apart, 64-dim slices 2 KiB apart
+            const uint64_t k_desc = tc05::sdesc(sbase, 16, C::KG_BYTES);
+            const uint64_t v_desc = tc05::sdesc(sbase + C::K_BYTES, 2048, 1024);
             auto issue_s = [&](int j) {
                 const uint64_t kst = k_desc + static_cast<uint64_t>((j % STAGES) * (C::STAGE_BYTES >> 4));
                 const uint32_t sd = tmem + C::S_COL + (j % NSB) * BN;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t b = kst + static_cast<uint64_t>(((ks >> 2) * C::KV_BOX + (ks & 3) * 32) >> 4);
+                    const uint64_t b = kst + static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4);
                     tc05::mma_ts(sd, tmem + C::Q_COL + ks * 8, b, ID_S, ks > 0);
                 }
                 tc05::commit(&s_full[j % NSB]);
@@ -206,8 +213,9 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
                 const uint32_t pa = tmem + C::S_COL + (j % NSB) * BN;  // key k at column k / 2
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    // N = D in one MMA: the four 64-dim boxes of V are KV_BOX apart (leading byte offset)
-                    const uint64_t b = vst + static_cast<uint64_t>((kk * 2048) >> 4);
+                    // N = D in one MMA (the four 64-dim slices 2 KiB apart: leading byte offset);
+                    // K-step kk is V sub-tile kk
+                    const uint64_t b = vst + static_cast<uint64_t>((kk * C::VS_BYTES) >> 4);
                     tc05::mma_ts(tmem + C::O_COL, pa + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc05::commit(o_ready);
@@ -357,8 +365,8 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
             for (int e = r; e < BN * NBOX * 8; e += 128) {
                 const int key = e / (NBOX * 8), rest = e % (NBOX * 8);
                 if (key0 + key >= L || !((okmask >> (key >> 4)) & 1))
-                    *reinterpret_cast<uint4*>(vt + (rest >> 3) * C::KV_BOX + key * 128 + (rest & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(vt + (key >> 4) * C::VS_BYTES + (rest >> 3) * 2048 + (key & 15) * 128 +
+                                              (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
         }
