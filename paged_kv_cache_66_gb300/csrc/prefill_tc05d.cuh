@@ -16,9 +16,10 @@
 //   softmax           one thread per row: tcgen05.ld of its 64 scores, causal mask, running
 //                     max, P_j = 2^(s - m) rounded to the dtype over the first half of S_j
 //   O += P_j . V_j    tcgen05.mma M=128 N=256, A = P_j (tensor memory), B = V_j (smem, MN-major)
-// The MMA issuer runs one tile ahead: S(j+1) as soon as K_(j+1) has landed (its
-// S buffer held P(j-1), whose P . V was issued before; one thread's MMAs run in
-// issue order), then P(j) . V_j once the softmax has written P(j).
+// The MMA issuer polls both inputs and issues whichever is ready: S(j+1) as soon
+// as K_(j+1) has landed (its S buffer held P(j-1), whose P . V was issued before;
+// one thread's MMAs run in issue order), P(j) . V_j once the softmax has written
+// P(j), so a P . V never waits behind a later tile's copy.
 // Warps: 0-3 softmax (thread = row = TMEM lane), 4 producer (TMA, four lanes
 // issuing), 5 MMA issuer.  Every wait is bounded (1 s); no barrier can run two
 // phases ahead of a waiter (comments at each wait); every warp-collective
@@ -188,38 +189,48 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
                 }
                 tc05::commit(&s_full[j % NSB]);
             };
-            // kv_full of tile j cannot complete another phase before kv_empty of tile j is
-            // committed (after its P . V, below), so each wait's parity is unambiguous
-            if (ok && n_kv > 0) {
-                ok = tc05::wait_bounded(&kv_full[0], 0);
-                if (ok) {
-                    tc05::fence_after();
-                    issue_s(0);
-                }
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    ok = tc05::wait_bounded(&kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1);
-                    if (!ok) break;
-                    tc05::fence_after();
-                    issue_s(j + 1);  // its S buffer held P(j-1), whose P . V was issued before
-                }
-                // P(j + NSB) needs S(j + NSB), issued after this P . V: at most one phase ahead
-                ok = tc05::wait_bounded(&p_full[j % NSB], (j / NSB) & 1);
-                if (!ok) break;
-                tc05::fence_after();
+            auto issue_pv = [&](int j) {
                 const int st = j % STAGES;
                 const uint64_t vst = v_desc + static_cast<uint64_t>(st * (C::STAGE_BYTES >> 4));
-                const uint32_t pa = tmem + C::S_COL + (j % NSB) * BN;  // key k at column k / 2
+                const uint32_t pt = tmem + C::S_COL + (j % NSB) * BN;  // key k at column k / 2
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     // N = D in one MMA (the four 64-dim slices 2 KiB apart: leading byte offset);
                     // K-step kk is V sub-tile kk
                     const uint64_t b = vst + static_cast<uint64_t>((kk * C::VS_BYTES) >> 4);
-                    tc05::mma_ts(tmem + C::O_COL, pa + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc05::mma_ts(tmem + C::O_COL, pt + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc05::commit(o_ready);
                 tc05::commit(&kv_empty[st]);  // the stage is free once this P . V completes
+            };
+            // S(ns) and P(np) . V go out as their inputs arrive, whichever is first, so that a P . V
+            // never waits behind a later tile's copy: S(ns) once K(ns) has landed and the P . V of
+            // the tile whose P its S buffer holds (ns - NSB) is issued; P(np) . V once the softmax
+            // has published P(np).  Parities: kv_full of tile j completes no other phase before
+            // kv_empty of tile j is committed (after its P . V), nor p_full of tile j before S(j + NSB)
+            // is issued (after P(j) . V).  No progress for 1 s ends the walk
+            int ns = 0, np = 0;
+            uint32_t idle = 0;
+            uint64_t t0 = 0;
+            while (ok && np < n_kv) {
+                bool moved = false;
+                if (ns < n_kv && ns < np + NSB && tc05::test_wait(&kv_full[ns % STAGES], (ns / STAGES) & 1)) {
+                    tc05::fence_after();
+                    issue_s(ns++);
+                    moved = true;
+                }
+                if (np < ns && tc05::test_wait(&p_full[np % NSB], (np / NSB) & 1)) {
+                    tc05::fence_after();
+                    issue_pv(np++);
+                    moved = true;
+                }
+                if (moved) {
+                    idle = 0;
+                } else if ((++idle & 255u) == 0) {
+                    const uint64_t t = global_timer_ns();
+                    if (idle == 256u) t0 = t;
+                    else if (t - t0 > 1000000000ull) ok = false;
+                }
             }
             if (ok) tc05::commit(o_final);
             else flag_error(p.err, PA_DEVERR_TIMEOUT);
