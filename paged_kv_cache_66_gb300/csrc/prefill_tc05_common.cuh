@@ -117,6 +117,13 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
     return mbar_wait_bounded(bar, parity, 1000000000ull, 2000u);
 }
 
+// true on one lane of the (converged, full) warp
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 

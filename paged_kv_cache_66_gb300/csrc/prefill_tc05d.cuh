@@ -167,71 +167,79 @@ __global__ void __launch_bounds__(Tc05dCfg::THREADS, 1)
     }
 
     if (warp == C::ISSUER) {
-        // ------------------------------------------------------------ MMA issuer (one lane)
-        if (lane == 0) {
-            constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
-            constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
-            // Q in tensor memory: written by the softmax threads (tcgen05.st) before q_full
-            bool ok = tc05::wait_bounded(q_full, 0);
-            tc05::fence_after();
-            // descriptors formed once; an operand at byte offset o from a base has the base's
-            // descriptor plus o / 16 (shared addresses stay below 2^18: no carry out of the field).
-            // K: 8-key groups KG_BYTES apart; V: 8-key groups 1 KiB apart, 64-dim slices 2 KiB apart
-            const uint64_t k_desc = tc05::sdesc(sbase, 16, C::KG_BYTES);
-            const uint64_t v_desc = tc05::sdesc(sbase + C::K_BYTES, 2048, 1024);
-            auto issue_s = [&](int j) {
-                const uint64_t kst = k_desc + static_cast<uint64_t>((j % STAGES) * (C::STAGE_BYTES >> 4));
-                const uint32_t sd = tmem + C::S_COL + (j % NSB) * BN;
+        // ------------------------------------------------------------ MMA issuer (one elected lane)
+        // The whole warp walks the issue loop, so operands are formed in warp-uniform code and only
+        // the MMAs and commits sit behind the elected lane: issued from a lane-0 branch instead, an
+        // N = 64 score MMA measured ~45 cycles against 32 (every decision below is warp-uniform)
+        const bool leader = tc05::elect_one();
+        constexpr uint32_t ID_S = tc05::idesc<T>(BN, false);
+        constexpr uint32_t ID_PV = tc05::idesc<T>(D, true);
+        // Q in tensor memory: written by the softmax threads (tcgen05.st) before q_full
+        bool ok = __all_sync(0xffffffffu, tc05::wait_bounded(q_full, 0));
+        tc05::fence_after();
+        // descriptors formed once; an operand at byte offset o from a base has the base's
+        // descriptor plus o / 16 (shared addresses stay below 2^18: no carry out of the field).
+        // K: 8-key groups KG_BYTES apart; V: 8-key groups 1 KiB apart, 64-dim slices 2 KiB apart
+        const uint64_t k_desc = tc05::sdesc(sbase, 16, C::KG_BYTES);
+        const uint64_t v_desc = tc05::sdesc(sbase + C::K_BYTES, 2048, 1024);
+        auto issue_s = [&](int j) {
+            const uint64_t kst = k_desc + static_cast<uint64_t>((j % STAGES) * (C::STAGE_BYTES >> 4));
+            const uint32_t sd = tmem + C::S_COL + (j % NSB) * BN;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t b = kst + static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4);
-                    tc05::mma_ts(sd, tmem + C::Q_COL + ks * 8, b, ID_S, ks > 0);
-                }
-                tc05::commit(&s_full[j % NSB]);
-            };
-            auto issue_pv = [&](int j) {
-                const int st = j % STAGES;
-                const uint64_t vst = v_desc + static_cast<uint64_t>(st * (C::STAGE_BYTES >> 4));
-                const uint32_t pt = tmem + C::S_COL + (j % NSB) * BN;  // key k at column k / 2
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t b = kst + static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4);
+                if (leader) tc05::mma_ts(sd, tmem + C::Q_COL + ks * 8, b, ID_S, ks > 0);
+            }
+            if (leader) tc05::commit(&s_full[j % NSB]);
+        };
+        auto issue_pv = [&](int j) {
+            const int st = j % STAGES;
+            const uint64_t vst = v_desc + static_cast<uint64_t>(st * (C::STAGE_BYTES >> 4));
+            const uint32_t pt = tmem + C::S_COL + (j % NSB) * BN;  // key k at column k / 2
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // N = D in one MMA (the four 64-dim slices 2 KiB apart: leading byte offset);
-                    // K-step kk is V sub-tile kk
-                    const uint64_t b = vst + static_cast<uint64_t>((kk * C::VS_BYTES) >> 4);
-                    tc05::mma_ts(tmem + C::O_COL, pt + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                // N = D in one MMA (the four 64-dim slices 2 KiB apart: leading byte offset);
+                // K-step kk is V sub-tile kk
+                const uint64_t b = vst + static_cast<uint64_t>((kk * C::VS_BYTES) >> 4);
+                if (leader) tc05::mma_ts(tmem + C::O_COL, pt + kk * 8, b, ID_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (leader) {
                 tc05::commit(o_ready);
                 tc05::commit(&kv_empty[st]);  // the stage is free once this P . V completes
-            };
-            // S(ns) and P(np) . V go out as their inputs arrive, whichever is first, so that a P . V
-            // never waits behind a later tile's copy: S(ns) once K(ns) has landed and the P . V of
-            // the tile whose P its S buffer holds (ns - NSB) is issued; P(np) . V once the softmax
-            // has published P(np).  Parities: kv_full of tile j completes no other phase before
-            // kv_empty of tile j is committed (after its P . V), nor p_full of tile j before S(j + NSB)
-            // is issued (after P(j) . V).  No progress for 1 s ends the walk
-            int ns = 0, np = 0;
-            uint32_t idle = 0;
-            uint64_t t0 = 0;
-            while (ok && np < n_kv) {
-                bool moved = false;
-                if (ns < n_kv && ns < np + NSB && tc05::test_wait(&kv_full[ns % STAGES], (ns / STAGES) & 1)) {
-                    tc05::fence_after();
-                    issue_s(ns++);
-                    moved = true;
-                }
-                if (np < ns && tc05::test_wait(&p_full[np % NSB], (np / NSB) & 1)) {
-                    tc05::fence_after();
-                    issue_pv(np++);
-                    moved = true;
-                }
-                if (moved) {
-                    idle = 0;
-                } else if ((++idle & 255u) == 0) {
-                    const uint64_t t = global_timer_ns();
-                    if (idle == 256u) t0 = t;
-                    else if (t - t0 > 1000000000ull) ok = false;
-                }
             }
+        };
+        // S(ns) and P(np) . V go out as their inputs arrive, whichever is first, so that a P . V
+        // never waits behind a later tile's copy: S(ns) once K(ns) has landed and the P . V of
+        // the tile whose P its S buffer holds (ns - NSB) is issued; P(np) . V once the softmax
+        // has published P(np).  Parities: kv_full of tile j completes no other phase before
+        // kv_empty of tile j is committed (after its P . V), nor p_full of tile j before S(j + NSB)
+        // is issued (after P(j) . V).  A phase counts as seen once every lane has seen it.  No
+        // progress for 1 s ends the walk
+        int ns = 0, np = 0;
+        uint32_t idle = 0;
+        uint64_t t0 = 0;
+        while (ok && np < n_kv) {
+            bool moved = false;
+            if (ns < n_kv && ns < np + NSB &&
+                __all_sync(0xffffffffu, tc05::test_wait(&kv_full[ns % STAGES], (ns / STAGES) & 1))) {
+                tc05::fence_after();
+                issue_s(ns++);
+                moved = true;
+            }
+            if (np < ns && __all_sync(0xffffffffu, tc05::test_wait(&p_full[np % NSB], (np / NSB) & 1))) {
+                tc05::fence_after();
+                issue_pv(np++);
+                moved = true;
+            }
+            if (moved) {
+                idle = 0;
+            } else if ((++idle & 255u) == 0) {
+                const uint64_t t = __shfl_sync(0xffffffffu, global_timer_ns(), 0);
+                if (idle == 256u) t0 = t;
+                else if (t - t0 > 1000000000ull) ok = false;
+            }
+        }
+        if (leader) {
             if (ok) tc05::commit(o_final);
             else flag_error(p.err, PA_DEVERR_TIMEOUT);
         }
