@@ -20,8 +20,11 @@
 // as K_(j+1) has landed (its S buffer held P(j-1), whose P . V was issued before;
 // one thread's MMAs run in issue order), P(j) . V_j once the softmax has written
 // P(j), so a P . V never waits behind a later tile's copy.
+// kmap / vmap are the pools' 3-D maps (element, row, 64-dim slice) with boxes of
+// 8 (K) and 16 (V) rows by every slice.
 // Warps: 0-3 softmax (thread = row = TMEM lane), 4 producer (TMA, four lanes
-// issuing), 5 MMA issuer.  Every wait is bounded (1 s); no barrier can run two
+// issuing), 5 MMA issuer (the whole warp walks the issue loop, one elected lane
+// issues the MMAs).  Every wait is bounded (1 s); no barrier can run two
 // phases ahead of a waiter (comments at each wait); every warp-collective
 // tcgen05 load / store sits behind warp-uniform decisions.
 #pragma once
