@@ -37,6 +37,26 @@ def test_library_exports_every_declared_symbol():
     assert set(names) == set(_lib.SIGNATURES), set(names) ^ set(_lib.SIGNATURES)
 
 
+@pytest.mark.parametrize("header", ["pagedkv.h", "pagedkv_host.h"])
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_public_headers_compile_standalone(header, lang, tmp_path):
+    """Each public header is self-contained, warning-free C11 and C++17 (no CUDA or torch types)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip(f"no {lang} compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text(f'#include "{header}"\n')
+    std = "-std=c11" if lang == "c" else "-std=c++17"
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    code = re.sub(r"/\*.*?\*/|//[^\n]*", "", open(os.path.join(ROOT, "include", header)).read(), flags=re.S)
+    assert not re.search(r"#include\s*[<\"](cuda|torch|ATen)|\bcuda\w*_t\b|\bCU\w+\b|\btorch\b|\bat::", code)
+
+
 def test_status_strings():
     lib = _lib.load()
     for code, name in _lib.STATUS_NAMES.items():
