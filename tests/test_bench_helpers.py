@@ -35,3 +35,16 @@ def test_algorithmic_bytes_of_the_fused_launch_add_the_new_rows():
 
 def test_cpu_model_is_reported():
     assert isinstance(bench._cpu_model(), str) and bench._cpu_model()
+
+
+def test_prefill_flop_count_is_the_brute_force_pair_count():
+    """The prefill metric counts 4 D Hq FLOPs per (query row, visible key) pair; the closed form of
+    the pair count equals a direct count of key positions k <= history + r over the chunk."""
+    for batch, history, chunk in [(1, 0, 1), (2, 0, 7), (3, 5, 4), (2, 33, 17)]:
+        wl = configs.prefill_config(batch=batch, history=history, chunk=chunk)
+        brute = batch * sum(1 for r in range(chunk) for k in range(history + chunk) if k <= history + r)
+        assert wl.causal_pairs() == brute
+    # the benchmark's 8 x 1024 over 3072: 8 (1024 * 3072 + 1024 * 1025 / 2) = 29 364 224 pairs per head
+    wl = configs.prefill_config()
+    assert wl.causal_pairs() == 29_364_224
+    assert 4 * wl.D * wl.Hq * wl.causal_pairs() == 481_103_446_016
